@@ -1,0 +1,46 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace dh {
+
+struct CoarseCall {
+  const void* x;
+  int64_t M, K;
+  const uint8_t* packed;
+  const void* S;
+  const void* ZS;
+  int64_t N;
+  int G, bits, kcand;
+  float* cand_val;
+  int32_t* cand_id;
+  void* y;
+  uint32_t* status;
+};
+
+struct RerankCall {
+  const void* x;
+  int64_t M, K;
+  const void* W;
+  int64_t N;
+  const float* cand_val;
+  const int32_t* cand_id;
+  int64_t ncand;
+  int R;
+  int32_t* rr_id;
+  float* rr_logit;
+  int32_t* argmax_id;
+  void* y;
+  uint32_t* status;
+};
+
+cudaError_t launch_quantize_pack(int bits, const void* W, int64_t N, int64_t K, int G,
+                                 uint8_t* packed, void* S, void* ZS, cudaStream_t s);
+// cudaErrorInvalidValue: the shape does not fit the kernel's shared-memory plan.
+cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s);
+cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s);
+
+}  // namespace dh

@@ -1,0 +1,230 @@
+// Global top-RERANK over the block candidates, exact rerank and argmax (page
+// "radiance_drafthead.py": bm.topk(RERANK) + bi.gather in _apply_head_int2, _rerank_exact with
+// bf16 rows, and the argmax its caller takes), for sm_103a.
+//
+// One CTA (1024 threads) per hidden row m:
+//  1. the row's candidates are held in registers (LPT per thread) as order-preserving keys;
+//  2. selection: R rounds, each taking the CTA-wide largest (value, then lowest id, then lowest
+//     slot index) and retiring it -- exact and deterministic, ties resolved as the sort that
+//     defines the operation;
+//  3. rerank: one warp per selected row, 16-byte loads of the bf16 weight row against the
+//     hidden row staged in shared memory, fp32 accumulation, xor-shuffle tree;
+//  4. argmax over the rescored values (ties to the lowest vocab id) and the optional scatter of
+//     bf16(logit) into the coarse logits.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dh_device.cuh"
+#include "dh_launch.h"
+
+namespace dh {
+
+constexpr int kRerankThreads = 1024;
+constexpr int kRerankWarps = kRerankThreads / 32;
+
+struct RerankArgs {
+  const uint16_t* x;  // bf16 [M, K]
+  int K, N;
+  const uint16_t* W;  // bf16 [N, K]
+  const float* cand_val;  // [M, ncand]
+  const int32_t* cand_id;
+  int ncand, R;
+  int32_t* rr_id;      // [M, R]
+  float* rr_logit;     // [M, R]
+  int32_t* argmax_id;  // [M]
+  uint16_t* y;         // bf16 [M, N] or nullptr
+  uint32_t* status;
+};
+
+// Selection order: key descending, then id ascending (as unsigned with the sign bit flipped),
+// then slot index ascending.
+struct Sel {
+  uint32_t key, uid, idx;
+};
+
+__device__ __forceinline__ bool sel_before(const Sel& a, const Sel& b) {
+  if (a.key != b.key) return a.key > b.key;
+  if (a.uid != b.uid) return a.uid < b.uid;
+  return a.idx < b.idx;
+}
+
+// Warp-wide best of one Sel per lane (all lanes get the result).
+__device__ __forceinline__ Sel warp_best(const Sel& s) {
+  Sel r;
+  r.key = __reduce_max_sync(0xffffffffu, s.key);
+  r.uid = __reduce_min_sync(0xffffffffu, s.key == r.key ? s.uid : 0xffffffffu);
+  r.idx = __reduce_min_sync(0xffffffffu, (s.key == r.key && s.uid == r.uid) ? s.idx : 0xffffffffu);
+  return r;
+}
+
+template <int LPT>
+__global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const RerankArgs a) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);                      // [K]
+  Sel* wbest = reinterpret_cast<Sel*>(sm + 2 * a.K);                    // [32]
+  Sel* chosen = wbest + kRerankWarps;                                   // [1]
+  int32_t* sel_id = reinterpret_cast<int32_t*>(chosen + 1);             // [R]
+  float* sel_logit = reinterpret_cast<float*>(sel_id + a.R);           // [R]
+  uint32_t* retired = reinterpret_cast<uint32_t*>(sel_logit + a.R);    // [ncand/32] (LPT == 0)
+
+  const int m = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint16_t* xrow = a.x + static_cast<int64_t>(m) * a.K;
+  for (int i = tid; i < a.K / 8; i += kRerankThreads)
+    reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(xrow)[i];
+
+  const float* cv = a.cand_val + static_cast<int64_t>(m) * a.ncand;
+  const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
+  // LPT > 0: this thread's candidates live in registers; LPT == 0: candidates are re-read from
+  // global memory every round and a shared bitmap marks the retired slots.
+  constexpr int kRegs = LPT > 0 ? LPT : 1;
+  uint32_t key[kRegs], uid[kRegs];
+  if (LPT == 0)
+    for (int i = tid; i < (a.ncand + 31) / 32; i += kRerankThreads) retired[i] = 0u;
+#pragma unroll
+  for (int j = 0; j < LPT; ++j) {
+    const int i = tid + j * kRerankThreads;
+    if (i < a.ncand) {
+      key[j] = order_key(cv[i]);
+      uid[j] = static_cast<uint32_t>(ci[i]) ^ 0x80000000u;
+    } else {
+      key[j] = 0u;
+      uid[j] = 0xffffffffu;
+    }
+  }
+
+  for (int r = 0; r < a.R; ++r) {
+    Sel best{0u, 0xffffffffu, 0xffffffffu};
+    if (LPT > 0) {
+#pragma unroll
+      for (int j = 0; j < kRegs; ++j) {
+        const Sel s{key[j], uid[j], static_cast<uint32_t>(tid + j * kRerankThreads)};
+        if (s.key != 0u && (best.key == 0u || sel_before(s, best))) best = s;
+      }
+    } else {
+      if (r == 0) __syncthreads();  // bitmap cleared
+      for (int i = tid; i < a.ncand; i += kRerankThreads) {
+        if (retired[i >> 5] & (1u << (i & 31))) continue;
+        const Sel s{order_key(cv[i]), static_cast<uint32_t>(ci[i]) ^ 0x80000000u,
+                    static_cast<uint32_t>(i)};
+        if (s.key != 0u && (best.key == 0u || sel_before(s, best))) best = s;
+      }
+    }
+    const Sel wb = warp_best(best);
+    if (lane == 0) wbest[warp] = wb;
+    __syncthreads();
+    if (warp == 0) {
+      const Sel fb = warp_best(wbest[lane]);
+      if (lane == 0) {
+        *chosen = fb;
+        sel_id[r] = static_cast<int32_t>(fb.uid ^ 0x80000000u);
+        if (LPT == 0 && fb.key != 0u) retired[fb.idx >> 5] |= 1u << (fb.idx & 31);
+      }
+    }
+    __syncthreads();
+    const uint32_t cidx = chosen->idx;
+    if (LPT > 0) {
+#pragma unroll
+      for (int j = 0; j < kRegs; ++j)
+        if (static_cast<uint32_t>(tid + j * kRerankThreads) == cidx) key[j] = 0u;
+    }
+  }
+  __syncthreads();
+
+  // exact rerank: one warp per selected row
+  for (int j = warp; j < a.R; j += kRerankWarps) {
+    const int n = sel_id[j];
+    float logit = -INFINITY;
+    if (n >= 0 && n < a.N) {
+      const uint4* wr = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(n) * a.K);
+      const uint4* xr = reinterpret_cast<const uint4*>(xs);
+      float acc = 0.0f;
+      for (int k8 = lane; k8 < a.K / 8; k8 += 32) {
+        const uint4 w8 = wr[k8];
+        const uint4 x8 = xr[k8];
+        const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
+        const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
+        float part = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          part = fmaf(__uint_as_float(xv[q] << 16), __uint_as_float(wv[q] << 16), part);
+          part = fmaf(__uint_as_float(xv[q] & 0xffff0000u), __uint_as_float(wv[q] & 0xffff0000u),
+                      part);
+        }
+        acc += part;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      logit = acc;
+    } else if (n >= a.N && lane == 0) {
+      set_status(a.status, DH_DEV_BAD_ID);
+    }
+    if (lane == 0) sel_logit[j] = logit;
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    uint32_t bk = 0u, bu = 0xffffffffu;
+    for (int j = lane; j < a.R; j += 32) {
+      const uint32_t k = order_key(sel_logit[j]);
+      const uint32_t u = static_cast<uint32_t>(sel_id[j]) ^ 0x80000000u;
+      if (k > bk || (k == bk && u < bu)) {
+        bk = k;
+        bu = u;
+      }
+    }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t umin = __reduce_min_sync(0xffffffffu, bk == kmax ? bu : 0xffffffffu);
+    if (lane == 0) a.argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+  }
+  for (int j = tid; j < a.R; j += kRerankThreads) {
+    a.rr_id[static_cast<int64_t>(m) * a.R + j] = sel_id[j];
+    a.rr_logit[static_cast<int64_t>(m) * a.R + j] = sel_logit[j];
+    const int n = sel_id[j];
+    if (a.y && n >= 0 && n < a.N)
+      a.y[static_cast<int64_t>(m) * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sel_logit[j]));
+  }
+}
+
+
+template <int LPT>
+static cudaError_t launch_rr(const RerankArgs& a, int M, cudaStream_t s) {
+  size_t smem = static_cast<size_t>(2 * a.K) + sizeof(Sel) * (kRerankWarps + 1) +
+                static_cast<size_t>(a.R) * 8;
+  if (LPT == 0) smem += 4 * static_cast<size_t>((a.ncand + 31) / 32);
+  cudaError_t e = cudaFuncSetAttribute(rerank_argmax_kernel<LPT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  rerank_argmax_kernel<LPT><<<M, kRerankThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s) {
+  RerankArgs a{};
+  a.x = static_cast<const uint16_t*>(rc.x);
+  a.K = static_cast<int>(rc.K);
+  a.N = static_cast<int>(rc.N);
+  a.W = static_cast<const uint16_t*>(rc.W);
+  a.cand_val = rc.cand_val;
+  a.cand_id = rc.cand_id;
+  a.ncand = static_cast<int>(rc.ncand);
+  a.R = rc.R;
+  a.rr_id = rc.rr_id;
+  a.rr_logit = rc.rr_logit;
+  a.argmax_id = rc.argmax_id;
+  a.y = static_cast<uint16_t*>(rc.y);
+  a.status = rc.status;
+  const int M = static_cast<int>(rc.M);
+  const int64_t per = (rc.ncand + kRerankThreads - 1) / kRerankThreads;
+  if (per <= 1) return launch_rr<1>(a, M, s);
+  if (per <= 2) return launch_rr<2>(a, M, s);
+  if (per <= 4) return launch_rr<4>(a, M, s);
+  if (per <= 8) return launch_rr<8>(a, M, s);
+  if (per <= 16) return launch_rr<16>(a, M, s);
+  return launch_rr<0>(a, M, s);
+}
+
+}  // namespace dh

@@ -1,0 +1,253 @@
+"""Python binding of the C ABI in include/drafthead.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch CUDA tensors for
+the device buffers, checks dtype / shape / contiguity, and passes raw pointers and the current
+CUDA stream to libdrafthead.so. PyTorch provides device memory and streams; every step of the
+draft head runs in the library's CUDA kernels. If the library has not been built the binding
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdrafthead.so")
+
+DH_OK = 0
+DH_ERR_NULL = -1
+DH_ERR_SHAPE = -2
+DH_ERR_ALIGN = -3
+DH_ERR_PARAM = -4
+DH_ERR_WORKSPACE = -5
+DH_ERR_CUDA = -6
+DH_ERR_DEVICE = -7
+DH_DEV_WAIT_TIMEOUT = 0x1
+DH_DEV_BAD_ID = 0x2
+BLOCK_ROWS = 64
+
+# C entry points and their argument types, in header order.
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "dh_quantize_pack_int2": ([_P, _I64, _I64, _I, _P, _P, _P, _P], _I),
+    "dh_quantize_pack_int4": ([_P, _I64, _I64, _I, _P, _P, _P, _P], _I),
+    "dh_packed_bytes": ([_I64, _I64, _I, _I], _SZ),
+    "dh_workspace_bytes": ([_I64, _I64, _I64, _I, _I], _SZ),
+    "dh_draft_head_coarse_topk": ([_P, _I64, _I64, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P,
+                                   _SZ, _P], _I),
+    "dh_draft_head_rerank_argmax": ([_P, _I64, _I64, _P, _I64, _P, _P, _I64, _I, _P, _P, _P, _P,
+                                     _P, _SZ, _P], _I),
+    "dh_workspace_status": ([_P, _SZ, _P, _P], _I),
+    "dh_last_error": ([], ctypes.c_char_p),
+}
+
+_lib = None
+
+
+class DraftHeadError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m bit_draft_lm_gb300.build` (nvcc, sm_103a)")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(h, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = h
+    return _lib
+
+
+def dh_last_error() -> str:
+    return lib().dh_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != DH_OK:
+        raise DraftHeadError(rc, dh_last_error())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype, shape=None) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype in (torch.int16, torch.uint16):
+        return t.view(torch.bfloat16)
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must hold bf16 values (torch.bfloat16), got {t.dtype}")
+    return t
+
+
+def dh_packed_bytes(N: int, K: int, G: int, bits: int) -> int:
+    return int(lib().dh_packed_bytes(N, K, G, bits))
+
+
+def dh_workspace_bytes(M: int, N: int, K: int, kcand: int, rerank: int) -> int:
+    return int(lib().dh_workspace_bytes(M, N, K, kcand, rerank))
+
+
+def new_workspace(M: int, N: int, K: int, kcand: int, rerank: int,
+                  device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for these sizes (the caching allocator aligns to 512 bytes)."""
+    n = dh_workspace_bytes(M, N, K, kcand, rerank)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _quantize(fn, bits, W, G, packed, S, ZS, stream):
+    W = _bf16(W, "W")
+    N, K = W.shape
+    per = 8 // bits
+    dev = W.device
+    if packed is None:
+        packed = torch.empty(N, K // per, dtype=torch.uint8, device=dev)
+    if S is None:
+        S = torch.empty(N, K // G, dtype=torch.bfloat16, device=dev)
+    if ZS is None:
+        ZS = torch.empty(N, K // G, dtype=torch.bfloat16, device=dev)
+    S, ZS = _bf16(S, "S"), _bf16(ZS, "ZS")
+    _check(fn(_dev(W, "W", torch.bfloat16), N, K, G,
+              _dev(packed, "packed", torch.uint8, (N, K // per)),
+              _dev(S, "S", torch.bfloat16, (N, K // G)), _dev(ZS, "ZS", torch.bfloat16, (N, K // G)),
+              _stream(stream)))
+    return packed, S, ZS
+
+
+def dh_quantize_pack_int2(W: torch.Tensor, G: int = 128, packed=None, S=None, ZS=None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    return _quantize(lib().dh_quantize_pack_int2, 2, W, G, packed, S, ZS, stream)
+
+
+def dh_quantize_pack_int4(W: torch.Tensor, G: int = 128, packed=None, S=None, ZS=None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    return _quantize(lib().dh_quantize_pack_int4, 4, W, G, packed, S, ZS, stream)
+
+
+def dh_draft_head_coarse_topk(x: torch.Tensor, packed: torch.Tensor, S: torch.Tensor,
+                              ZS: torch.Tensor, N: int, G: int = 128, bits: int = 2,
+                              kcand: int = 8, cand_val=None, cand_id=None, y_coarse=None,
+                              workspace=None, stream=None):
+    """-> (cand_val f32 [M, nblk*kcand], cand_id i32 [M, nblk*kcand])."""
+    x = _bf16(x, "x")
+    M, K = x.shape
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    dev = x.device
+    if cand_val is None:
+        cand_val = torch.empty(M, nblk * kcand, dtype=torch.float32, device=dev)
+    if cand_id is None:
+        cand_id = torch.empty(M, nblk * kcand, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(M, N, K, kcand, 1, dev)
+    if y_coarse is not None:
+        y_coarse = _bf16(y_coarse, "y_coarse")
+    _check(lib().dh_draft_head_coarse_topk(
+        _dev(x, "x", torch.bfloat16), M, K, _dev(packed, "packed", torch.uint8),
+        _dev(_bf16(S, "S"), "S", torch.bfloat16), _dev(_bf16(ZS, "ZS"), "ZS", torch.bfloat16),
+        N, G, bits, kcand,
+        _dev(cand_val, "cand_val", torch.float32, (M, nblk * kcand)),
+        _dev(cand_id, "cand_id", torch.int32, (M, nblk * kcand)),
+        _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    return cand_val, cand_id
+
+
+def dh_draft_head_rerank_argmax(x: torch.Tensor, W: torch.Tensor, cand_val: torch.Tensor,
+                                cand_id: torch.Tensor, rerank: int = 16, rr_id=None,
+                                rr_logit=None, argmax_id=None, y_coarse=None, workspace=None,
+                                stream=None):
+    """-> (rr_id i32 [M, R], rr_logit f32 [M, R], argmax_id i32 [M])."""
+    x = _bf16(x, "x")
+    W = _bf16(W, "W")
+    M, K = x.shape
+    N = W.shape[0]
+    ncand = cand_val.shape[1]
+    dev = x.device
+    if rr_id is None:
+        rr_id = torch.empty(M, rerank, dtype=torch.int32, device=dev)
+    if rr_logit is None:
+        rr_logit = torch.empty(M, rerank, dtype=torch.float32, device=dev)
+    if argmax_id is None:
+        argmax_id = torch.empty(M, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(M, N, K, 1, rerank, dev)
+    if y_coarse is not None:
+        y_coarse = _bf16(y_coarse, "y_coarse")
+    _check(lib().dh_draft_head_rerank_argmax(
+        _dev(x, "x", torch.bfloat16), M, K, _dev(W, "W", torch.bfloat16, (N, K)), N,
+        _dev(cand_val, "cand_val", torch.float32, (M, ncand)),
+        _dev(cand_id, "cand_id", torch.int32, (M, ncand)), ncand, rerank,
+        _dev(rr_id, "rr_id", torch.int32, (M, rerank)),
+        _dev(rr_logit, "rr_logit", torch.float32, (M, rerank)),
+        _dev(argmax_id, "argmax_id", torch.int32, (M,)),
+        _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    return rr_id, rr_logit, argmax_id
+
+
+def dh_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the workspace status word (0 = no kernel failure)."""
+    word = ctypes.c_uint32(0)
+    rc = lib().dh_workspace_status(_dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                                   ctypes.addressof(word), _stream(stream))
+    if rc not in (DH_OK, DH_ERR_DEVICE):
+        _check(rc)
+    return int(word.value)
+
+
+class DraftHead:
+    """A quantised draft head on one GPU: the bf16 weight W[N, K] (kept for the exact rerank)
+    plus its int2/int4 packing, and a workspace; calling it runs the whole path for x[M, K]."""
+
+    def __init__(self, W: torch.Tensor, G: int = 128, bits: int = 2, kcand: int = 8,
+                 rerank: int = 16, max_tokens: int = 72):
+        W = _bf16(W, "W")
+        if not W.is_cuda:
+            raise ValueError("W must be a CUDA tensor")
+        self.W, self.G, self.bits, self.kcand, self.rerank = W, G, bits, kcand, rerank
+        self.N, self.K = W.shape
+        quant = dh_quantize_pack_int2 if bits == 2 else dh_quantize_pack_int4
+        self.packed, self.S, self.ZS = quant(W, G)
+        self.workspace = new_workspace(max_tokens, self.N, self.K, kcand, rerank, W.device)
+        self.max_tokens = max_tokens
+
+    def __call__(self, x: torch.Tensor, y_coarse=None, stream=None):
+        """x bf16 [M, K] on the device -> dict of argmax [M], rr_id [M, R], rr_logit [M, R],
+        cand_val, cand_id."""
+        if x.shape[0] > self.max_tokens:
+            raise ValueError(f"M={x.shape[0]} > max_tokens={self.max_tokens}")
+        cv, ci = dh_draft_head_coarse_topk(x, self.packed, self.S, self.ZS, self.N, self.G,
+                                           self.bits, self.kcand, y_coarse=y_coarse,
+                                           workspace=self.workspace, stream=stream)
+        rr, rl, am = dh_draft_head_rerank_argmax(x, self.W, cv, ci, self.rerank,
+                                                 y_coarse=y_coarse, workspace=self.workspace,
+                                                 stream=stream)
+        return {"argmax": am, "rr_id": rr, "rr_logit": rl, "cand_val": cv, "cand_id": ci}

@@ -91,8 +91,18 @@ def _pick_pairs(rng: np.random.Generator, N: int, planted: np.ndarray) -> np.nda
 
 
 def make_workload(M: int, K: int, N: int, seed: int, rms_norm: bool = True,
-                  lognormal_rows: bool = True, name: str = "") -> Workload:
-    """Draw one workload; see the module docstring for the recipe."""
+                  lognormal_rows: bool = True, name: str = "", plant: bool = True) -> Workload:
+    """Draw one workload; see the module docstring for the recipe. ``plant=False`` skips the
+    planted rows and near-tie pairs (for very small N)."""
+    if not plant:
+        rng = np.random.default_rng(seed)
+        z = rng.standard_normal((M, K))
+        if rms_norm:
+            z = z / np.sqrt(np.mean(z * z, axis=1, keepdims=True))
+        scale = 0.02 * (np.exp(0.3 * rng.standard_normal(N)) if lognormal_rows else np.ones(N))
+        W = bf16_bits(rng.standard_normal((N, K)) * scale[:, None])
+        return Workload(name or f"M{M}_K{K}_N{N}_s{seed}_plain", M, K, N, seed, bf16_bits(z), W,
+                        np.zeros(0, dtype=np.int64), np.zeros((0, 2), dtype=np.int64), 0)
     if N < 2 * BLOCK_ROWS or N < N_PLANTED + N_PAIRS:
         raise ValueError("N too small for the planting recipe")
     rng = np.random.default_rng(seed)

@@ -1,0 +1,145 @@
+/*
+ * drafthead.h -- C ABI of the GB300 (sm_103a) low-bit speculative-decoding draft head.
+ *
+ * The operation is the draft head of the page "radiance_drafthead.py" (module docstring;
+ * _quantize_head_now, _draft_head_int2, _emit, _rerank_exact, _apply_head_int2):
+ *   logits = x[M, K] @ W^T for a vocabulary head W[N, K] (vocab rows, the lm_head layout),
+ * computed coarsely from int2 (or int4) codes with an asymmetric per-(vocab row, group of G
+ * along K) scale and zero point, after which each 64-row block keeps its KCAND largest coarse
+ * values, the RERANK largest of those are rescored exactly against the bf16 weight, and the
+ * argmax of the rescored logits is returned per hidden row.
+ *
+ * Conventions (every entry point):
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the library allocates no
+ *    device memory and keeps no tensors. Inputs are never written.
+ *  - bf16 tensors are passed as `void*` / `const void*` and hold IEEE bfloat16 bit patterns.
+ *  - Every layout is dense row-major with the stated shape (no strides).
+ *  - Calls are asynchronous and stream-ordered on `s` (NULL = the legacy default stream). The
+ *    return value reports argument validation and launch errors only (cudaGetLastError is read
+ *    without synchronising); failures detected inside a kernel are recorded in the workspace
+ *    status word (see dh_workspace_status). No call synchronises the device or allocates, so
+ *    the per-call entry points can be captured in a CUDA graph.
+ *  - On any non-OK return nothing was launched; dh_last_error() gives a message.
+ *  - Pointers read with 16-byte vector loads must be 16-byte aligned (DH_ERR_ALIGN otherwise).
+ */
+#ifndef DRAFTHEAD_H_
+#define DRAFTHEAD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dh_stream_t; /* the same handle as cudaStream_t */
+
+#define DH_BLOCK_ROWS 64   /* BLOCK_N of the page: vocab rows per candidate block */
+#define DH_MAX_KCAND 64    /* candidates kept per block (at most the block width) */
+#define DH_MAX_RERANK 256  /* largest RERANK accepted */
+#define DH_MAX_TOKENS 4096 /* largest M accepted */
+
+enum {
+  DH_OK = 0,
+  DH_ERR_NULL = -1,      /* a required pointer is NULL */
+  DH_ERR_SHAPE = -2,     /* sizes out of range or not divisible as required */
+  DH_ERR_ALIGN = -3,     /* a pointer is not aligned as required */
+  DH_ERR_PARAM = -4,     /* G, bits, kcand or rerank not supported */
+  DH_ERR_WORKSPACE = -5, /* workspace NULL, misaligned or smaller than dh_workspace_bytes */
+  DH_ERR_CUDA = -6,      /* a CUDA runtime call or a launch failed */
+  DH_ERR_DEVICE = -7     /* returned by dh_workspace_status when a kernel flagged a failure */
+};
+
+/* Bits of the workspace status word (set by kernels, never cleared by the library). */
+#define DH_DEV_WAIT_TIMEOUT 0x1u /* a bounded wait inside the coarse kernel ran out; outputs invalid */
+#define DH_DEV_BAD_ID 0x2u       /* the rerank met a candidate id >= N; that slot scored -inf */
+
+/*
+ * Offline quantise + pack, int2 (_quantize_head_now with BITS = 2; docstring "Quarter-split
+ * packing" and "Bit-pattern dequant, hoisted").
+ *   W       bf16 [N, K], the head weight, vocab rows.                              (16-B aligned)
+ *   G       group size along K: 64 or 128.  Requires K % (4*G) == 0.
+ *   packed  u8 [N, K/4] out: byte j of row n = q[j] | q[Q+j]<<2 | q[2Q+j]<<4 | q[3Q+j]<<6, Q=K/4.
+ *   S       bf16 [N, K/G] out: bf16(4*sc).
+ *   ZS      bf16 [N, K/G] out: bf16(4*sc + zp*sc).
+ * with, per (row, group): sc = max((hi-lo)/3, 1e-8), zp = clamp(round(-lo/sc), 0, 3),
+ * q = clamp(round(w/sc + zp), 0, 3) in IEEE fp32 (round = half to even).
+ */
+int dh_quantize_pack_int2(const void* W, int64_t N, int64_t K, int G, uint8_t* packed, void* S,
+                          void* ZS, dh_stream_t s);
+
+/*
+ * The 4-bit comparison variant ("as in the 4-bit path"; packing q[:, :K/2] | q[:, K/2:] << 4,
+ * premultiplier 16): requires K % (2*G) == 0; packed u8 [N, K/2]; S = bf16(16 sc),
+ * ZS = bf16(16 sc + zp sc); codes 0..15.
+ */
+int dh_quantize_pack_int4(const void* W, int64_t N, int64_t K, int G, uint8_t* packed, void* S,
+                          void* ZS, dh_stream_t s);
+
+/* Bytes of packed + S + ZS for one head (0 for unsupported arguments). For N=124160, K=5120,
+ * G=128, bits=2 this is 178,790,400 (the page's 0.167 GiB/rank). */
+size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits);
+
+/* Workspace bytes the two per-call entry points need for these sizes (one workspace serves
+ * both). The workspace must be zero-filled once before first use; calls sharing a workspace
+ * must be ordered on one stream. */
+size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank);
+
+/*
+ * Coarse pass + block top-KCAND (_draft_head_int2 followed by _emit).
+ *   x         bf16 [M, K] hidden states, 1 <= M <= DH_MAX_TOKENS.                  (16-B aligned)
+ *   packed,S,ZS  as written by dh_quantize_pack_int2 (bits=2) or _int4 (bits=4).  (16-B aligned)
+ *   G         64 or 128; requires K % (8*G) == 0 and K <= 5120.
+ *   kcand     1..DH_MAX_KCAND candidates per 64-row block.
+ *   cand_val  f32 [M, nblk*kcand] out, nblk = ceil(N/64): for hidden row m and block b,
+ *             slots b*kcand .. b*kcand+kcand-1 hold the kcand largest coarse values
+ *             c[m, n] = sum_g ( S[n,g] * sum_{k in g} x[m,k] (1 + v[n,k]/beta) - ZS[n,g] * sum_{k in g} x[m,k] )
+ *             (beta = 4 for int2, 16 for int4), descending, equal values by ascending row id;
+ *             slots past the block's last valid row hold (-inf, -1).
+ *   cand_id   i32 [M, nblk*kcand] out: the vocab row of each slot.
+ *   y_coarse  bf16 [M, N] out or NULL: bf16(c), the coarse logits.
+ *   workspace device buffer of ws_bytes >= dh_workspace_bytes(...), 256-B aligned.
+ */
+int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                              const void* S, const void* ZS, int64_t N, int G, int bits,
+                              int kcand, float* cand_val, int32_t* cand_id, void* y_coarse,
+                              void* workspace, size_t ws_bytes, dh_stream_t s);
+
+/*
+ * Global top-RERANK over the block candidates, exact rerank, argmax (bm.topk + bi.gather,
+ * _rerank_exact with bf16 rows, then the caller's argmax).
+ *   x         bf16 [M, K] (the same hidden states).                                (16-B aligned)
+ *   W         bf16 [N, K] the exact head weight.                                   (16-B aligned)
+ *   cand_val, cand_id  f32 / i32 [M, ncand] (any candidate list; ncand >= rerank).
+ *   rerank    1..DH_MAX_RERANK.
+ *   rr_id     i32 [M, rerank] out: the rerank largest candidates, ordered by candidate value
+ *             descending then id ascending (one entry per candidate slot).
+ *   rr_logit  f32 [M, rerank] out: sum_k x[m,k] W[rr_id,k] accumulated in fp32 (-inf for an
+ *             id < 0; an id >= N also scores -inf and sets DH_DEV_BAD_ID).
+ *   argmax_id i32 [M] out: the rr_id with the largest rr_logit, equal logits by lowest id
+ *             (-1 when every slot is empty).
+ *   y_coarse  bf16 [M, N] in/out or NULL: when given, y[m, rr_id] = bf16(rr_logit) (the
+ *             page's scatter of the exact values over the coarse logits).
+ *   workspace as for the coarse call.
+ */
+int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void* W, int64_t N,
+                                const float* cand_val, const int32_t* cand_id, int64_t ncand,
+                                int rerank, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                                void* y_coarse, void* workspace, size_t ws_bytes, dh_stream_t s);
+
+/*
+ * Synchronises `s`, copies the workspace status word to *device_status and returns DH_OK if
+ * it is zero, DH_ERR_DEVICE otherwise (DH_ERR_CUDA if the copy fails). The word is sticky:
+ * zero the workspace to clear it.
+ */
+int dh_workspace_status(const void* workspace, size_t ws_bytes, uint32_t* device_status,
+                        dh_stream_t s);
+
+/* Message for the last non-OK status returned on the calling host thread ("" if none). */
+const char* dh_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DRAFTHEAD_H_ */

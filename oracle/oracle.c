@@ -228,13 +228,19 @@ static void coarse_rows(void* p, int64_t lo_row, int64_t hi_row) {
       for (int64_t gi = 0; gi < ng; ++gi) {
         const double s = (double)bf16_to_float(c->S[n * ng + gi]);
         const double zs = (double)bf16_to_float(c->ZS[n * ng + gi]);
-        double pg = 0.0, xs = 0.0, dv = 0.0;
-        for (int64_t k = gi * G; k < gi * G + G; ++k) {
-          pg += xv[k] * d[k];
-          xs += xv[k];
-          dv += xv[k] * ((s / beta) * (double)v[k] - (zs - s));
+        if (c->dequant_form) {
+          double dv = 0.0;
+          for (int64_t k = gi * G; k < gi * G + G; ++k)
+            dv += xv[k] * ((s / beta) * (double)v[k] - (zs - s));
+          acc += dv;
+        } else {
+          double pg = 0.0, xs = 0.0;
+          for (int64_t k = gi * G; k < gi * G + G; ++k) {
+            pg += xv[k] * d[k];
+            xs += xv[k];
+          }
+          acc += s * pg - zs * xs;
         }
-        acc += c->dequant_form ? dv : (s * pg - zs * xs);
       }
       c->out[m * N + n] = acc;
     }

@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library builds, loads and exports every entry point declared in
+include/drafthead.h, and rejects bad arguments on the host before any CUDA call.
+
+Every call below fails validation, so no kernel is launched and no pointer is dereferenced
+(the fake addresses are never touched).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_draft_lm_gb300 import build as dh_build
+from bit_draft_lm_gb300 import drafthead as dh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "drafthead.h")
+
+A16 = 0x10000          # fake, 16-byte aligned address (never dereferenced)
+A256 = 0x20000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dh_build.build()
+    return dh.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dh_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = _declared()
+    assert "dh_draft_head_coarse_topk" in names and "dh_quantize_pack_int2" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(dh.SIGNATURES), "binding and header disagree"
+
+
+def test_packed_bytes_page_shape(lib):
+    assert dh.dh_packed_bytes(124160, 5120, 128, 2) == 178_790_400
+    assert dh.dh_packed_bytes(124160, 5120, 64, 2) == 158_924_800 + 2 * 124160 * 80 * 2
+    assert dh.dh_packed_bytes(124160, 5120, 128, 4) == 124160 * 2560 + 2 * 124160 * 40 * 2
+    assert dh.dh_packed_bytes(10, 100, 128, 2) == 0
+    assert dh.dh_packed_bytes(10, 1024, 96, 2) == 0
+    assert dh.dh_workspace_bytes(8, 124160, 5120, 8, 16) >= 256
+
+
+def _quant(lib, W=A16, N=64, K=1024, G=128, packed=A16, S=A16, ZS=A16, bits=2):
+    f = lib.dh_quantize_pack_int2 if bits == 2 else lib.dh_quantize_pack_int4
+    return f(W, N, K, G, packed, S, ZS, None)
+
+
+def test_quantize_validation(lib):
+    assert _quant(lib, W=None) == dh.DH_ERR_NULL
+    assert "NULL" in dh.dh_last_error()
+    assert _quant(lib, G=96) == dh.DH_ERR_PARAM
+    assert _quant(lib, K=1000) == dh.DH_ERR_SHAPE
+    assert _quant(lib, K=256 + 512) == dh.DH_ERR_SHAPE          # not a multiple of 4*G
+    assert _quant(lib, K=640, bits=4) == dh.DH_ERR_SHAPE         # int4 needs K % (2G)
+    assert _quant(lib, N=0) == dh.DH_ERR_SHAPE
+    assert _quant(lib, W=A16 + 2) == dh.DH_ERR_ALIGN
+
+
+def _coarse(lib, x=A16, M=1, K=1024, packed=A16, S=A16, ZS=A16, N=8192, G=128, bits=2,
+            kcand=8, cv=A16, ci=A16, y=None, ws=A256, wsb=256):
+    return lib.dh_draft_head_coarse_topk(x, M, K, packed, S, ZS, N, G, bits, kcand, cv, ci, y, ws,
+                                         wsb, None)
+
+
+def test_coarse_validation(lib):
+    assert _coarse(lib, x=None) == dh.DH_ERR_NULL
+    assert _coarse(lib, cv=None) == dh.DH_ERR_NULL
+    assert _coarse(lib, bits=3) == dh.DH_ERR_PARAM
+    assert _coarse(lib, G=32) == dh.DH_ERR_PARAM
+    assert _coarse(lib, kcand=0) == dh.DH_ERR_PARAM
+    assert _coarse(lib, kcand=65) == dh.DH_ERR_PARAM
+    assert _coarse(lib, M=0) == dh.DH_ERR_SHAPE
+    assert _coarse(lib, M=5000) == dh.DH_ERR_SHAPE
+    assert _coarse(lib, N=0) == dh.DH_ERR_SHAPE
+    assert _coarse(lib, K=1536) == dh.DH_ERR_SHAPE              # not a multiple of 8*G
+    assert _coarse(lib, K=6144) == dh.DH_ERR_SHAPE              # above the supported K
+    assert _coarse(lib, x=A16 + 8) == dh.DH_ERR_ALIGN
+    assert _coarse(lib, packed=A16 + 4) == dh.DH_ERR_ALIGN
+    assert _coarse(lib, cv=A16 + 2) == dh.DH_ERR_ALIGN
+    assert _coarse(lib, ws=None) == dh.DH_ERR_WORKSPACE
+    assert _coarse(lib, ws=A256 + 64) == dh.DH_ERR_WORKSPACE
+    assert _coarse(lib, wsb=16) == dh.DH_ERR_WORKSPACE
+    assert "workspace" in dh.dh_last_error()
+
+
+def _rerank(lib, x=A16, M=1, K=1024, W=A16, N=8192, cv=A16, ci=A16, ncand=1024, R=16, rr=A16,
+            rl=A16, am=A16, y=None, ws=A256, wsb=256):
+    return lib.dh_draft_head_rerank_argmax(x, M, K, W, N, cv, ci, ncand, R, rr, rl, am, y, ws,
+                                           wsb, None)
+
+
+def test_rerank_validation(lib):
+    assert _rerank(lib, W=None) == dh.DH_ERR_NULL
+    assert _rerank(lib, am=None) == dh.DH_ERR_NULL
+    assert _rerank(lib, R=0) == dh.DH_ERR_PARAM
+    assert _rerank(lib, R=257) == dh.DH_ERR_PARAM
+    assert _rerank(lib, ncand=8, R=16) == dh.DH_ERR_SHAPE        # rerank > ncand
+    assert _rerank(lib, K=1001) == dh.DH_ERR_SHAPE
+    assert _rerank(lib, M=0) == dh.DH_ERR_SHAPE
+    assert _rerank(lib, W=A16 + 8) == dh.DH_ERR_ALIGN
+    assert _rerank(lib, rr=A16 + 1) == dh.DH_ERR_ALIGN
+    assert _rerank(lib, wsb=0) == dh.DH_ERR_WORKSPACE
+
+
+def test_status_validation(lib):
+    word = ctypes.c_uint32(0)
+    assert lib.dh_workspace_status(None, 256, ctypes.addressof(word), None) == dh.DH_ERR_NULL
+    assert lib.dh_workspace_status(A256, 0, ctypes.addressof(word), None) == dh.DH_ERR_WORKSPACE
+
+
+def test_last_error_cleared_by_success_path_message(lib):
+    _coarse(lib, G=7)
+    assert "G=7" in dh.dh_last_error()

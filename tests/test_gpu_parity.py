@@ -1,0 +1,271 @@
+"""GPU parity against the CPU oracle, through the C ABI (libdrafthead.so via the binding).
+
+Quantiser bytes and scales: bit-exact. Block candidates: ids exact up to near-ties, values within
+the coarse tolerance. Rerank: ids exact (same candidate lists in, same total order), logits within
+the rerank tolerance, argmax equal on every non-tied row. See tests/_parity.py for the bars.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_draft_lm_gb300 import build as dh_build
+from bit_draft_lm_gb300 import drafthead as dh
+from bit_draft_lm_gb300 import synth
+
+from _parity import (bf16_to_f64, check_block_candidates, coarse_tol, dev_bf16, host_u16,
+                     near_tie_rows, rerank_tol)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    dh_build.build()
+    dh.lib()
+
+
+def _gpu_quant(W_u16, G, bits):
+    W = dev_bf16(W_u16)
+    f = dh.dh_quantize_pack_int2 if bits == 2 else dh.dh_quantize_pack_int4
+    packed, S, ZS = f(W, G)
+    torch.cuda.synchronize()
+    return W, packed, S, ZS
+
+
+QUANT_CASES = [
+    (8192, 1024, 128, 2, 0),
+    (1000, 2048, 64, 2, 21),
+    (777, 1024, 128, 4, 22),
+    (300, 5120, 64, 4, 23),
+    (129, 5120, 128, 2, 24),
+]
+
+
+@pytest.mark.parametrize("N,K,G,bits,seed", QUANT_CASES)
+def test_quantize_bit_exact(N, K, G, bits, seed):
+    w = synth.make_workload(1, K, N, seed, plant=N >= 128)
+    W = w.W.copy()
+    W[0] = 0                                    # constant (zero) row: sc clamps to 1e-8
+    W[1] = synth.bf16_bits(np.full(K, 0.75))    # constant non-zero row
+    _, packed, S, ZS = _gpu_quant(W, G, bits)
+    op, oS, oZS = oracle.quantize_pack(W, G, bits)
+    assert np.array_equal(packed.cpu().numpy(), op)
+    assert np.array_equal(host_u16(S), oS)
+    assert np.array_equal(host_u16(ZS), oZS)
+
+
+COARSE_CASES = [
+    # M, K, N, G, bits, kcand, seed
+    (1, 1024, 8192, 128, 2, 8, 0),      # the small draft head
+    (3, 1024, 8232, 128, 2, 8, 10),     # ragged N: partial last block and tile
+    (8, 2048, 4100, 64, 2, 8, 11),      # G = 64
+    (13, 1024, 3000, 128, 2, 5, 12),    # M > 8 (two passes), odd KCAND
+    (5, 1024, 2048, 128, 4, 1, 13),     # int4, KCAND = 1
+    (8, 2048, 2048, 64, 4, 8, 14),      # int4, G = 64 (fold per 64-byte sub-chunk)
+    (2, 5120, 4096, 128, 2, 64, 15),    # K = 5120 (20 consumer warps), KCAND = 64
+    (1, 1024, 70, 128, 2, 8, 16),       # two blocks, the second with 6 rows
+]
+
+
+def _run_case(M, K, N, G, bits, kcand, seed, with_y=True):
+    w = synth.make_workload(M, K, N, seed, plant=N >= 128)
+    W, packed, S, ZS = _gpu_quant(w.W, G, bits)
+    x = dev_bf16(w.x)
+    y = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda") if with_y else None
+    ws = dh.new_workspace(M, N, K, kcand, 16)
+    cv, ci = dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, G, bits, kcand, y_coarse=y,
+                                          workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.dh_workspace_status(ws) == 0
+    op, oS, oZS = oracle.quantize_pack(w.W, G, bits)
+    c = oracle.coarse(w.x, op, oS, oZS, G, bits)
+    ov, oi = oracle.block_topk(c, kcand)
+    return w, (W, packed, S, ZS, x, y, ws, cv, ci), c, ov, oi
+
+
+@pytest.mark.parametrize("M,K,N,G,bits,kcand,seed", COARSE_CASES)
+def test_coarse_topk_parity(M, K, N, G, bits, kcand, seed):
+    w, dev, c, ov, oi = _run_case(M, K, N, G, bits, kcand, seed)
+    _, _, _, _, _, y, _, cv, ci = dev
+    mism = check_block_candidates(c, ov, oi, cv.cpu().numpy(), ci.cpu().numpy(), kcand)
+    assert mism <= max(2, ov.size // 1000), f"{mism} near-tie swaps"
+    # coarse logits: bf16(c) within the coarse tolerance plus half a bf16 step
+    yv = bf16_to_f64(host_u16(y))
+    assert np.all(np.abs(yv - c) <= coarse_tol(c) + np.abs(c) * 2.0 ** -8)
+
+
+def _rand_candidates(rng, M, ncand, N, tie_levels=None):
+    val = rng.standard_normal((M, ncand)).astype(np.float32)
+    if tie_levels:
+        val = (np.round(val * tie_levels) / tie_levels).astype(np.float32)
+    ids = np.stack([rng.choice(N, ncand, replace=False) for _ in range(M)]).astype(np.int32)
+    return val, ids
+
+
+RERANK_CASES = [
+    # M, K, N, ncand, R, ties, seed
+    (1, 1024, 8192, 1024, 16, None, 30),
+    (4, 2048, 20000, 5000, 16, 4, 31),     # many exact value ties
+    (3, 1024, 40000, 20000, 16, None, 32),  # more candidates than registers hold
+    (2, 1024, 8192, 64, 64, 2, 33),         # R = ncand
+    (5, 5120, 4096, 300, 1, None, 34),      # R = 1
+    (2, 1024, 8192, 3000, 256, None, 35),   # R = 256
+]
+
+
+@pytest.mark.parametrize("M,K,N,ncand,R,ties,seed", RERANK_CASES)
+def test_rerank_argmax_parity(M, K, N, ncand, R, ties, seed):
+    rng = np.random.default_rng(seed)
+    w = synth.make_workload(M, K, N, seed, plant=False)
+    val, ids = _rand_candidates(rng, M, ncand, N, ties)
+    # some empty slots, as short blocks produce
+    val[:, -3:] = -np.inf
+    ids[:, -3:] = -1
+    x, W = dev_bf16(w.x), dev_bf16(w.W)
+    ws = dh.new_workspace(M, N, K, 1, R)
+    rr, rl, am = dh.dh_draft_head_rerank_argmax(
+        x, W, torch.from_numpy(val).cuda(), torch.from_numpy(ids).cuda(), R, workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.dh_workspace_status(ws) == 0
+    o_rr, _ = oracle.global_topr(val.astype(np.float64), ids, R)
+    assert np.array_equal(rr.cpu().numpy(), o_rr)
+    e = oracle.rerank(w.x, w.W, o_rr)
+    gl = rl.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(e)
+    assert np.array_equal(np.isfinite(gl), fin)
+    tol = rerank_tol(w.x, w.W, o_rr, e)
+    assert np.all(np.abs(gl[fin] - e[fin]) <= tol[fin])
+    o_am = oracle.argmax(e, o_rr)
+    ok = ~near_tie_rows(e)
+    assert np.array_equal(am.cpu().numpy()[ok], o_am[ok])
+
+
+E2E_CASES = [
+    (1, 1024, 8192, 128, 2, 8, 16, 0),
+    (3, 1024, 8232, 128, 2, 8, 16, 10),
+    (13, 1024, 3000, 128, 2, 5, 16, 12),
+    (5, 1024, 2048, 128, 4, 1, 16, 13),
+    (4, 5120, 8192, 128, 2, 8, 32, 17),
+]
+
+
+@pytest.mark.parametrize("M,K,N,G,bits,kcand,R,seed", E2E_CASES)
+def test_end_to_end_parity(M, K, N, G, bits, kcand, R, seed):
+    w, dev, c, ov, oi = _run_case(M, K, N, G, bits, kcand, seed, with_y=False)
+    W, packed, S, ZS, x, _, ws, cv, ci = dev
+    rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, workspace=ws)
+    torch.cuda.synchronize()
+    o_rr, _ = oracle.global_topr(ov, oi, R)
+    e_o = oracle.rerank(w.x, w.W, o_rr)
+    o_am = oracle.argmax(e_o, o_rr)
+    g_rr = rr.cpu().numpy()
+    # ids: exact except where near-tied coarse values swap at the top-R boundary
+    tol = coarse_tol(c)
+    for m in range(M):
+        if not np.array_equal(g_rr[m], o_rr[m]):
+            d = g_rr[m] != o_rr[m]
+            assert np.all(np.abs(c[m, g_rr[m][d]] - c[m, o_rr[m][d]]) <=
+                          np.maximum(tol[m, g_rr[m][d]], tol[m, o_rr[m][d]]))
+    e_g = oracle.rerank(w.x, w.W, g_rr)
+    gl = rl.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(gl - e_g) <= rerank_tol(w.x, w.W, g_rr, e_g))
+    ok = ~near_tie_rows(e_o)
+    assert np.array_equal(am.cpu().numpy()[ok], o_am[ok])
+    # the method's claim on the planted workloads: reranked argmax = brute-force exact argmax
+    if N >= 128 and bits == 2:
+        ex = oracle.exact_logits(w.x[:1], w.W)
+        assert int(am[0]) == int(np.argmax(ex[0]))
+
+
+def test_scatter_into_coarse_logits():
+    M, K, N, G, kcand, R = 2, 1024, 8192, 128, 8, 16
+    w, dev, c, ov, oi = _run_case(M, K, N, G, 2, kcand, 40)
+    W, packed, S, ZS, x, y, ws, cv, ci = dev
+    y_before = y.clone()
+    rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, y_coarse=y, workspace=ws)
+    torch.cuda.synchronize()
+    rr, rl = rr.cpu().long(), rl.cpu()
+    yh, yb = y.float().cpu(), y_before.float().cpu()
+    for m in range(M):
+        assert torch.equal(yh[m, rr[m]], rl[m].to(torch.bfloat16).float())
+        mask = torch.ones(N, dtype=torch.bool)
+        mask[rr[m]] = False
+        assert torch.equal(yh[m, mask], yb[m, mask])
+
+
+def test_inputs_unmodified_and_deterministic():
+    M, K, N, G, kcand, R = 8, 2048, 4096, 128, 8, 16
+    w = synth.make_workload(M, K, N, 41)
+    W, packed, S, ZS = _gpu_quant(w.W, G, 2)
+    x = dev_bf16(w.x)
+    snap = [t.clone() for t in (W, packed, S, ZS, x)]
+    head = []
+    for _ in range(2):
+        ws = dh.new_workspace(M, N, K, kcand, R)
+        cv, ci = dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, G, 2, kcand, workspace=ws)
+        rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, workspace=ws)
+        torch.cuda.synchronize()
+        head.append([t.clone() for t in (cv, ci, rr, rl, am)])
+    for a, b in zip(snap, (W, packed, S, ZS, x)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    for a, b in zip(*head):
+        assert torch.equal(a, b)
+
+
+def test_side_stream_and_graph_capture():
+    M, K, N, G, kcand, R = 4, 1024, 8192, 128, 8, 16
+    w = synth.make_workload(M, K, N, 42)
+    W, packed, S, ZS = _gpu_quant(w.W, G, 2)
+    x = dev_bf16(w.x)
+    ws = dh.new_workspace(M, N, K, kcand, R)
+    ref = None
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        cv, ci = dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, G, 2, kcand, workspace=ws)
+        rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, workspace=ws)
+    s.synchronize()
+    ref = [t.clone() for t in (cv, ci, rr, rl, am)]
+    for t in (cv, ci, rr, rl, am):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, G, 2, kcand, cand_val=cv, cand_id=ci,
+                                     workspace=ws)
+        dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, rr_id=rr, rr_logit=rl, argmax_id=am,
+                                       workspace=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, (cv, ci, rr, rl, am)):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["head_m1_k5120_n124160", "head_m8_k5120_n124160"])
+def test_vocabulary_scale_parity(name):
+    """The full vocabulary shard (K=5120, N=124160): quantiser bit-exact on every row, block
+    candidates of every row and block, and the argmax, against the full oracle."""
+    w = synth.named(name)
+    M, K, N, G, kcand, R = w.M, w.K, w.N, 128, 8, 16
+    W, packed, S, ZS = _gpu_quant(w.W, G, 2)
+    op, oS, oZS = oracle.quantize_pack(w.W, G, 2)
+    assert np.array_equal(packed.cpu().numpy(), op)
+    assert np.array_equal(host_u16(S), oS) and np.array_equal(host_u16(ZS), oZS)
+    x = dev_bf16(w.x)
+    ws = dh.new_workspace(M, N, K, kcand, R)
+    cv, ci = dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, G, 2, kcand, workspace=ws)
+    rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.dh_workspace_status(ws) == 0
+    c = oracle.coarse(w.x, op, oS, oZS, G, 2)
+    ov, oi = oracle.block_topk(c, kcand)
+    mism = check_block_candidates(c, ov, oi, cv.cpu().numpy(), ci.cpu().numpy(), kcand)
+    assert mism <= ov.size // 1000
+    o_rr, _ = oracle.global_topr(ov, oi, R)
+    e_o = oracle.rerank(w.x, w.W, o_rr)
+    o_am = oracle.argmax(e_o, o_rr)
+    ok = ~near_tie_rows(e_o)
+    assert np.array_equal(am.cpu().numpy()[ok], o_am[ok])
+    ex = oracle.exact_logits(w.x, w.W)
+    assert int(am[0]) == int(np.argmax(ex[0]))
