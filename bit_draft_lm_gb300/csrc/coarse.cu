@@ -18,7 +18,7 @@
 //    byte j and byte j+2 of a 32-bit word share one bf16x2 register; x is permuted the same way.
 //  * The per-group scale is applied to the accumulator, never to the weight tile:
 //    acc += S[n,g] * P_g per (plane, strip) and acc -= sum_g ZS[n,g] * XS[m,g] once per tile as a
-//    short MMA whose B operand is -XS split into bf16 hi + lo parts (K' = 2*K/G).
+//    short MMA whose B operand is -XS split into three bf16 parts (K' = 3*K/G, padded to 16).
 //  * Block epilogue: partial accumulators of the NW warps are summed in a fixed order (the
 //    result does not depend on timing), then warp m selects the KCAND largest of the block's 64
 //    coarse values for hidden row m with warp reductions (max key, then lowest row on ties).
@@ -187,19 +187,24 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     if (lane == 0) xs_s[tok * KG + gi] = sum;
   }
   named_bar_sync(1, nthr);
-  uint2* xsfrag = reinterpret_cast<uint2*>(sm + a.off_xsfrag);  // [KG/8][32]
-  for (int e = threadIdx.x; e < (KG / 8) * 32; e += nthr) {
+  // -XS as three bf16 parts (hi + mid + lo, relative error 2^-27): virtual column vk of the ZS
+  // term's MMA is part vk / KG of group vk % KG; columns past 3*KG are zero padding.
+  const int zs_steps = (3 * KG + 15) / 16;
+  uint2* xsfrag = reinterpret_cast<uint2*>(sm + a.off_xsfrag);  // [zs_steps][32]
+  for (int e = threadIdx.x; e < zs_steps * 32; e += nthr) {
     const int ks = e >> 5, l = e & 31, gg = l >> 2, cc = l & 3;
     uint32_t h[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int vk = 16 * ks + 2 * cc + (q & 1) + (q >> 1) * 8;
-      const bool lo_part = vk >= KG;
-      const int gi = lo_part ? vk - KG : vk;
-      const float v = gg < a.mt ? xs_s[gg * KG + gi] : 0.0f;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-      h[q] = static_cast<uint32_t>(__bfloat16_as_ushort(lo_part ? lo : hi)) ^ 0x8000u;  // -XS
+      const int part = vk / KG, gi = vk - part * KG;
+      float v = (gg < a.mt && part < 3) ? xs_s[gg * KG + gi] : 0.0f;
+      __nv_bfloat16 pv = __float2bfloat16_rn(v);
+      for (int t = 0; t < part; ++t) {  // peel off the parts above this one
+        v -= __bfloat162float(pv);
+        pv = __float2bfloat16_rn(v);
+      }
+      h[q] = static_cast<uint32_t>(__bfloat16_as_ushort(pv)) ^ 0x8000u;  // -XS part
     }
     xsfrag[e] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
   }
@@ -264,9 +269,8 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
       if (warp == (t * NW) / kTilesPerBlock) {
         const unsigned char* zst = st + a.zs_off;
         const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;
-        for (int ks = 0; ks < KG / 8; ++ks) {
-          int col = 16 * ks + 8 * (lane >> 4);
-          col = col >= KG ? col - KG : col;
+        for (int ks = 0; ks < zs_steps; ++ks) {
+          const int col = (16 * ks + 8 * (lane >> 4)) % KG;  // B is zero past 3*KG
           uint32_t z0, z1, z2, z3;
           ldmatrix_x4(z0, z1, z2, z3, zst + (lr * KG + col) * 2);
           const uint2 xb = xsfrag[ks * 32 + lane];
@@ -309,8 +313,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
       }
     }
     named_bar_sync(1, nthr);
-    if (warp < a.mt) {
-      const int m = warp;
+    for (int m = warp; m < a.mt; m += NW) {
       const int n0 = b * kBlockRows + lane;
       uint32_t k0 = n0 < a.N ? order_key(blk[lane * kBlkPitch + m]) : 0u;
       uint32_t k1 = n0 + 32 < a.N ? order_key(blk[(lane + 32) * kBlkPitch + m]) : 0u;
@@ -363,7 +366,7 @@ static bool plan_coarse(CoarseArgs& a, int bits, int max_smem) {
   a.off_red = off;
   off += a.NW * kTilesPerBlock * 32 * 16;
   a.off_xsfrag = off;
-  off += (a.KG / 8) * 32 * 8;
+  off += ((3 * a.KG + 15) / 16) * 32 * 8;
   a.off_xs = off;
   off += 8 * a.KG * 4;
   a.off_blk = off;

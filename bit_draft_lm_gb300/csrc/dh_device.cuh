@@ -18,10 +18,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) {
   return __uint_as_float(h << 16);
 }
 
-// Total order on fp32 as unsigned keys: larger float -> larger key (-0 < +0). Key 0 is only
-// produced by the NaN with all bits set, so 0 serves as "no candidate".
+// Total order on fp32 as unsigned keys: larger float -> larger key; -0 and +0 map to the same
+// key (they compare equal). Key 0 is only produced by the NaN with all bits set, so 0 serves as
+// "no candidate".
 __device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
+  uint32_t u = f == 0.0f ? 0u : __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ float key_to_float(uint32_t k) {
