@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 int2 draft head: one pass of the hot path (coarse int2 pass + block
+top-KCAND, then global top-RERANK + exact bf16 rerank + argmax) per step, on the vocabulary-scale
+head (K=5120, N=124160, G=128, KCAND=8, RERANK=16), hidden rows M=1 by default.
+
+Prints ONE JSON line. Timing: CUDA events on the launching stream after warm-up, synchronised
+on both sides; the packed weight, scales and bf16 weight rotate over 4 device copies (716 MB of
+packed head, 5 GB of bf16 head) so every step reads its weights from HBM, not from the 129 MB
+L2. `--impl reference` times the CPU oracle (the plain fp64 statement of the method) on the same
+workload instead. Multi-GPU (torchrun): every rank runs an independent replica (the head does
+not shard here); value = job-level microseconds per call over all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+K_DIM, N_VOCAB, GROUP, KCAND, RERANK = 5120, 124160, 128, 8, 16
+COPIES = 4
+METRIC = "draft-head us/call + achieved HBM GB/s vs ~8 TB/s, M=1/8/72, K=5120 N=124160"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "coarse_traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--m", type=int, default=1, help="hidden rows of the headline workload")
+    p.add_argument("--extra-m", default="8,72", help="supplementary row counts ('' = none)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-soak", action="store_true",
+                   help="skip the 1.5 s clock-sampling soak (profiling runs)")
+    p.add_argument("--copies", type=int, default=COPIES,
+                   help="rotating weight copies (4 keep every step out of L2)")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------------ helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def coarse_source_hash():
+    h = hashlib.sha256()
+    for f in ("coarse.cu", "dh_device.cuh"):
+        with open(os.path.join(ROOT, "bit_draft_lm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(M):
+    """dram bytes per coarse launch from the committed ncu summary, if it was taken on the
+    current kernel source and this row count; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        if d.get("source_hash") == coarse_source_hash() and int(d.get("M", -1)) == M:
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons while the GPU runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip() == "Active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ workload
+def workload_host(M, seed=1):
+    """x [M, K] and W [N, K] bf16 bits: the vocabulary-scale recipe of synth (row 0 of x and the
+    planted rows / near-tie pairs of W follow the recipe; further rows of x are fresh draws)."""
+    from bit_draft_lm_gb300 import synth
+    w = synth.named("head_m1_k5120_n124160")
+    rng = np.random.default_rng(seed + 1000 + M)
+    z = rng.standard_normal((max(M, 1) * COPIES, K_DIM))
+    z /= np.sqrt(np.mean(z * z, axis=1, keepdims=True))
+    xs = synth.bf16_bits(z).reshape(COPIES, max(M, 1), K_DIM)
+    xs[0, 0] = w.x[0]
+    return xs, w.W
+
+
+# ------------------------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from bit_draft_lm_gb300 import build as dh_build
+    from bit_draft_lm_gb300 import drafthead as dh
+
+    dh_build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    xs_h, W_h = workload_host(max([args.m] + extra_ms(args)))
+    W0 = torch.from_numpy(W_h.view(np.int16)).to(dev).view(torch.bfloat16)
+    ncopy = max(1, args.copies)
+    Ws = [W0] + [W0.clone() for _ in range(ncopy - 1)]
+    packs = [dh.dh_quantize_pack_int2(Wc, GROUP) for Wc in Ws]
+    torch.cuda.synchronize()
+    nblk = (N_VOCAB + 63) // 64
+
+    def measure(M, steps, warmup, record_launches):
+        xs = [torch.from_numpy(xs_h[c, :M].copy().view(np.int16)).to(dev).view(torch.bfloat16)
+              for c in range(ncopy)]
+        ws = dh.new_workspace(M, N_VOCAB, K_DIM, KCAND, RERANK, dev)
+        cv = torch.empty(M, nblk * KCAND, dtype=torch.float32, device=dev)
+        ci = torch.empty(M, nblk * KCAND, dtype=torch.int32, device=dev)
+        rr = torch.empty(M, RERANK, dtype=torch.int32, device=dev)
+        rl = torch.empty(M, RERANK, dtype=torch.float32, device=dev)
+        am = torch.empty(M, dtype=torch.int32, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step(i, ev=None):
+            c = i % ncopy
+            p, S, ZS = packs[c]
+            if ev is not None:
+                ev[0].record(stream)
+            dh.dh_draft_head_coarse_topk(xs[c], p, S, ZS, N_VOCAB, GROUP, 2, KCAND, cand_val=cv,
+                                         cand_id=ci, workspace=ws)
+            if ev is not None:
+                ev[1].record(stream)
+            dh.dh_draft_head_rerank_argmax(xs[c], Ws[c], cv, ci, RERANK, rr_id=rr, rr_logit=rl,
+                                           argmax_id=am, workspace=ws)
+
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)] if record_launches else [None] * steps
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(steps):
+            step(i, evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = t0.elapsed_time(t1)
+        coarse_ms = [a.elapsed_time(b) for a, b in evs] if record_launches else []
+        status = dh.dh_workspace_status(ws)
+        if status:
+            raise RuntimeError(f"kernel status word {status:#x}")
+        return ms, coarse_ms
+
+    clocks = ClockSampler(dev.index)
+    time.sleep(0.3)
+    ms, coarse_ms = measure(args.m, args.steps, max(args.warmup, 3), True)
+    # keep the same step running ~1.5 s so the clock samples cover this workload under load
+    soak_t = time.time()
+    if not args.no_soak:
+        soak_steps = max(1, int(1.5e3 / max(ms / args.steps, 1e-3)))
+        measure(args.m, min(soak_steps, 200000), 3, False)
+    soak_t = time.time() - soak_t
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    us_step = ms * 1e3 / args.steps
+    coarse_us = 1e3 * statistics.fmean(coarse_ms)
+    peak, peak_kind = measured_peaks()
+    alg_coarse = dh.dh_packed_bytes(N_VOCAB, K_DIM, GROUP, 2)
+    alg_call = alg_coarse + args.m * RERANK * K_DIM * 2
+    launches_per_step = (args.m + 7) // 8 + 1
+
+    extra = {}
+    for M in extra_ms(args):
+        steps = max(50, min(args.steps, int(3e5 / max(M, 1))))
+        mm, cm = measure(M, steps, 5, True)
+        u = mm * 1e3 / steps
+        extra[str(M)] = {"us_per_call": round(u, 3),
+                         "coarse_us": round(1e3 * statistics.fmean(cm), 3),
+                         "hbm_gbs_per_call": round((alg_coarse + M * RERANK * K_DIM * 2) / u / 1e3, 1),
+                         "steps": steps}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, dev, Ws, xs_h, ncopy)
+
+    line = {
+        "metric": METRIC,
+        "value": round(us_step / world, 3),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms / args.steps, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy: RMS-normed N(0,1) hidden rows; lognormal-row N(0,0.02) "
+                "head with planted rows and near-tie pairs)",
+        "config": {"workload": f"int2 draft head M={args.m} K={K_DIM} N={N_VOCAB} G={GROUP} "
+                               f"KCAND={KCAND} RERANK={RERANK}",
+                   "M": args.m, "K": K_DIM, "N": N_VOCAB, "G": GROUP, "bits": 2,
+                   "kcand": KCAND, "rerank": RERANK,
+                   "l2": f"inputs larger than L2: {ncopy} rotating copies of the packed head "
+                         f"({ncopy * alg_coarse / 1e6:.0f} MB) and of the bf16 head",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs_per_call": round(alg_call / us_step / 1e3, 1),
+        "roofline": {"bound": "hbm", "kernel": "coarse_topk_kernel",
+                     "achieved": round(alg_coarse / coarse_us / 1e3, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(alg_coarse / coarse_us / 1e3 / peak, 4),
+                     "peak_kind": peak_kind,
+                     "traffic": profiled_traffic(args.m),
+                     "algorithmic_bytes_per_launch": alg_coarse,
+                     "launch_us": round(coarse_us, 3)},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": dict(clk, window=f"timed region + {soak_t:.1f} s of the same step"),
+        "per_m": extra,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args.m, budget_s=15.0)
+    return line
+
+
+def extra_ms(args):
+    return [int(v) for v in args.extra_m.split(",") if v.strip()] if args.extra_m else []
+
+
+def run_e2e(args, dev, Ws, xs_h, ncopy):
+    """The public API from host memory: DraftHead.infer copies x from pinned host memory, runs
+    the head and reads argmax / rr_id / rr_logit back, synchronising every step."""
+    import torch
+    from bit_draft_lm_gb300 import drafthead as dh
+    M = args.m
+    heads = [dh.DraftHead(Wc, GROUP, 2, KCAND, RERANK, max_tokens=M) for Wc in Ws]
+    xh = [torch.from_numpy(xs_h[c, :M].copy().view(np.int16)).view(torch.bfloat16).pin_memory()
+          for c in range(ncopy)]
+    torch.cuda.synchronize()
+    for i in range(max(args.warmup, 3)):
+        heads[i % ncopy].infer(xh[i % ncopy])
+    steps = min(args.steps, 2000)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        heads[i % ncopy].infer(xh[i % ncopy])
+    dt = time.perf_counter() - t0
+    return {"value": round(dt * 1e6 / steps, 3), "unit": "us/call",
+            "h2d_bytes_per_step": M * K_DIM * 2,
+            "d2h_bytes_per_step": M * 4 + 2 * M * RERANK * 4, "steps": steps}
+
+
+# ------------------------------------------------------------------------------------ oracle arm
+def oracle_sample(M, rows):
+    """Quantise a slice of the head with the oracle (untimed) and return a callable running the
+    oracle's full path (coarse -> block top-K -> top-R -> rerank -> argmax) on that slice."""
+    import oracle
+    xs_h, W_h = workload_host(M)
+    Ws = np.ascontiguousarray(W_h[:rows])
+    x = np.ascontiguousarray(xs_h[0, :M])
+    packed, S, ZS = oracle.quantize_pack(Ws, GROUP, 2)
+
+    def call():
+        return oracle.head(x, packed, S, ZS, Ws, G=GROUP, bits=2, kcand=KCAND, R=RERANK)
+    return call
+
+
+def cpu_baseline(M, budget_s):
+    """The oracle as it stands, on the host cores, on a bounded slice of the same head; time per
+    call scaled to the full vocabulary (the slice's rows are a fixed fraction of N)."""
+    import oracle
+    rows = 15520                                # 1/8 of the vocabulary, whole 64-row blocks
+    call = oracle_sample(M, rows)
+    call()
+    times = []
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s or len(times) < 3:
+        t0 = time.perf_counter()
+        call()
+        times.append(time.perf_counter() - t0)
+        if len(times) >= 50:
+            break
+    scale = N_VOCAB / rows
+    return {"value": round(statistics.median(times) * scale * 1e6, 1), "unit": "us/call",
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{len(times)} calls of the oracle's full path on a {rows}-row slice "
+                      f"(1/{int(scale)}) of the N={N_VOCAB} head at M={M}, median x {scale:g}"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed per step on a bounded slice of the workload."""
+    import oracle
+    probe = oracle_sample(args.m, 1940)
+    t0 = time.perf_counter()
+    probe()
+    t_small = max(time.perf_counter() - t0, 1e-4)
+    per_step_budget = 120.0 / max(args.steps + args.warmup, 1)
+    rows = int(1940 * per_step_budget / t_small) // 64 * 64
+    rows = max(128, min(rows, N_VOCAB // 4))
+    call = probe if rows == 1940 else oracle_sample(args.m, rows)
+    for _ in range(args.warmup):
+        call()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        call()
+        times.append(time.perf_counter() - t0)
+    scale = N_VOCAB / rows
+    v = statistics.fmean(times) * scale * 1e6
+    sample = (f"each step: the oracle's full path on a {rows}-row slice of the N={N_VOCAB} head "
+              f"at M={args.m}, time x {scale:.3g}")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/call",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"int2 draft head M={args.m} K={K_DIM} N={N_VOCAB} G={GROUP} "
+                                   f"KCAND={KCAND} RERANK={RERANK}", "M": args.m},
+            "cpu_baseline": {"value": round(v, 1), "unit": "us/call", "cores": oracle.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -4,11 +4,14 @@
 //
 // One CTA (1024 threads) per hidden row m:
 //  1. the row's candidates are held in registers (LPT per thread) as order-preserving keys;
-//  2. selection: R rounds, each taking the CTA-wide largest (value, then lowest id, then lowest
-//     slot index) and retiring it -- exact and deterministic, ties resolved as the sort that
-//     defines the operation;
-//  3. rerank: one warp per selected row, 16-byte loads of the bf16 weight row against the
-//     hidden row staged in shared memory, fp32 accumulation, xor-shuffle tree;
+//  2. selection, exact and deterministic (order: value descending, then lowest id, then lowest
+//     slot index, i.e. the sort that defines the operation): a threshold T that provably lies
+//     at or below the R-th largest value filters the candidates, the survivors are compacted to
+//     shared memory and one warp sorts (<= 32) or selects (<= 256) them; with more survivors
+//     (heavy ties) or R > 32, R rounds each retire the CTA-wide first remaining candidate;
+//  3. rerank: 32/R warps per selected row over slices of K, 16-byte loads of the bf16 weight
+//     row against the hidden row staged in shared memory, fp32 accumulation, xor-shuffle tree,
+//     slice sums added in a fixed order;
 //  4. argmax over the rescored values (ties to the lowest vocab id) and the optional scatter of
 //     bf16(logit) into the coarse logits.
 #include <cuda_bf16.h>
@@ -59,6 +62,28 @@ __device__ __forceinline__ Sel warp_best(const Sel& s) {
   return r;
 }
 
+// Bitonic sort of one Sel per lane across the warp: lane 0 ends with the first in selection
+// order. Empty lanes carry key 0 and sort last.
+__device__ __forceinline__ Sel warp_sort(Sel v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      Sel o;
+      o.key = __shfl_xor_sync(0xffffffffu, v.key, j);
+      o.uid = __shfl_xor_sync(0xffffffffu, v.uid, j);
+      o.idx = __shfl_xor_sync(0xffffffffu, v.idx, j);
+      const bool keep_first = ((lane & j) == 0) == ((lane & k) == 0);
+      const bool o_first = sel_before(o, v);
+      if (keep_first == o_first) v = o;
+    }
+  }
+  return v;
+}
+
+constexpr int kSurvivorCap = 256;  // candidates the one-warp exact selection takes after the filter
+
 template <int LPT>
 __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const RerankArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
@@ -67,7 +92,10 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
   Sel* chosen = wbest + kRerankWarps;                                   // [1]
   int32_t* sel_id = reinterpret_cast<int32_t*>(chosen + 1);             // [R]
   float* sel_logit = reinterpret_cast<float*>(sel_id + a.R);           // [R]
-  uint32_t* retired = reinterpret_cast<uint32_t*>(sel_logit + a.R);    // [ncand/32] (LPT == 0)
+  float* part_logit = sel_logit + a.R;                                  // [R * wpr]
+  Sel* surv = reinterpret_cast<Sel*>(part_logit + a.R * kRerankWarps);  // [kSurvivorCap]
+  uint32_t* wtmp = reinterpret_cast<uint32_t*>(surv + kSurvivorCap);    // [32 + 2]
+  uint32_t* retired = wtmp + kRerankWarps + 2;                          // [ncand/32] (LPT == 0)
 
   const int m = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -79,36 +107,114 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
   const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
   // LPT > 0: this thread's candidates live in registers; LPT == 0: candidates are re-read from
   // global memory every round and a shared bitmap marks the retired slots.
+  // Only the keys stay in registers; ids are re-read (L1/L2) where a tie-break or a result
+  // needs them.
   constexpr int kRegs = LPT > 0 ? LPT : 1;
-  uint32_t key[kRegs], uid[kRegs];
+  uint32_t key[kRegs];
+  auto uid_at = [&](int i) { return static_cast<uint32_t>(ci[i]) ^ 0x80000000u; };
   if (LPT == 0)
     for (int i = tid; i < (a.ncand + 31) / 32; i += kRerankThreads) retired[i] = 0u;
 #pragma unroll
   for (int j = 0; j < LPT; ++j) {
     const int i = tid + j * kRerankThreads;
-    if (i < a.ncand) {
-      key[j] = order_key(cv[i]);
-      uid[j] = static_cast<uint32_t>(ci[i]) ^ 0x80000000u;
-    } else {
-      key[j] = 0u;
-      uid[j] = 0xffffffffu;
-    }
+    key[j] = i < a.ncand ? order_key(cv[i]) : 0u;
   }
 
-  for (int r = 0; r < a.R; ++r) {
+  // Fast exact path. T = the R-th largest of the 32 warp maxima is at most the R-th largest
+  // candidate (those R maxima are R distinct candidates >= T), so every member of the top R has
+  // key >= T. Items >= T are compacted into shared memory and one warp selects among them.
+  bool selected = false;
+  if (LPT > 0 && a.R <= 32) {
+    uint32_t tmax = 0u;
+#pragma unroll
+    for (int j = 0; j < kRegs; ++j) tmax = max(tmax, key[j]);
+    tmax = __reduce_max_sync(0xffffffffu, tmax);
+    if (lane == 0) wtmp[warp] = tmax;
+    __syncthreads();
+    if (warp == 0) {
+      const Sel w = warp_sort(Sel{wtmp[lane], 0u, static_cast<uint32_t>(lane)});
+      const uint32_t T = __shfl_sync(0xffffffffu, w.key, a.R - 1);
+      if (lane == 0) wtmp[kRerankWarps] = T;
+    }
+    __syncthreads();
+    const uint32_t T = wtmp[kRerankWarps];
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < kRegs; ++j) cnt += (key[j] != 0u && key[j] >= T) ? 1 : 0;
+    int incl = cnt;  // warp inclusive scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __syncthreads();  // every thread has read T before wtmp is reused
+    if (lane == 31) wtmp[warp] = static_cast<uint32_t>(incl);
+    __syncthreads();
+    if (warp == 0) {
+      int wsum = static_cast<int>(wtmp[lane]);
+      int wincl = wsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += v;
+      }
+      __syncwarp();
+      wtmp[lane] = static_cast<uint32_t>(wincl - wsum);  // exclusive warp base
+      if (lane == 31) wtmp[kRerankWarps + 1] = static_cast<uint32_t>(wincl);
+    }
+    __syncthreads();
+    const int total = static_cast<int>(wtmp[kRerankWarps + 1]);
+    if (total <= kSurvivorCap) {
+      int pos = static_cast<int>(wtmp[warp]) + incl - cnt;
+#pragma unroll
+      for (int j = 0; j < kRegs; ++j)
+        if (key[j] != 0u && key[j] >= T) {
+          const int i = tid + j * kRerankThreads;
+          surv[pos++] = Sel{key[j], uid_at(i), static_cast<uint32_t>(i)};
+        }
+    }
+    __syncthreads();
+    if (total <= kSurvivorCap) {
+      selected = true;
+      if (warp == 0) {
+        if (total <= 32) {
+          Sel v = lane < total ? surv[lane] : Sel{0u, 0xffffffffu, 0xffffffffu};
+          v = warp_sort(v);
+          if (lane < a.R) sel_id[lane] = static_cast<int32_t>(v.uid ^ 0x80000000u);
+        } else {
+          for (int r = 0; r < a.R; ++r) {
+            Sel best{0u, 0xffffffffu, 0xffffffffu};
+            for (int q = lane; q < total; q += 32) {
+              const Sel v = surv[q];
+              if (v.key != 0u && (best.key == 0u || sel_before(v, best))) best = v;
+            }
+            const Sel wb = warp_best(best);
+            for (int q = lane; q < total; q += 32)
+              if (surv[q].key != 0u && surv[q].idx == wb.idx) surv[q].key = 0u;
+            __syncwarp();
+            if (lane == 0) sel_id[r] = static_cast<int32_t>(wb.uid ^ 0x80000000u);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  for (int r = 0; r < (selected ? 0 : a.R); ++r) {
     Sel best{0u, 0xffffffffu, 0xffffffffu};
     if (LPT > 0) {
 #pragma unroll
       for (int j = 0; j < kRegs; ++j) {
-        const Sel s{key[j], uid[j], static_cast<uint32_t>(tid + j * kRerankThreads)};
-        if (s.key != 0u && (best.key == 0u || sel_before(s, best))) best = s;
+        if (key[j] == 0u || (best.key != 0u && key[j] < best.key)) continue;
+        const int i = tid + j * kRerankThreads;
+        const Sel s{key[j], uid_at(i), static_cast<uint32_t>(i)};
+        if (best.key == 0u || sel_before(s, best)) best = s;
       }
     } else {
       if (r == 0) __syncthreads();  // bitmap cleared
       for (int i = tid; i < a.ncand; i += kRerankThreads) {
         if (retired[i >> 5] & (1u << (i & 31))) continue;
-        const Sel s{order_key(cv[i]), static_cast<uint32_t>(ci[i]) ^ 0x80000000u,
-                    static_cast<uint32_t>(i)};
+        const Sel s{order_key(cv[i]), uid_at(i), static_cast<uint32_t>(i)};
         if (s.key != 0u && (best.key == 0u || sel_before(s, best))) best = s;
       }
     }
@@ -133,15 +239,21 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
   }
   __syncthreads();
 
-  // exact rerank: one warp per selected row
-  for (int j = warp; j < a.R; j += kRerankWarps) {
+  // exact rerank: wpr warps per selected row, each over a contiguous K range; the partial sums
+  // are added in a fixed order
+  int wpr = 1;
+  while (wpr * 2 * a.R <= kRerankWarps && wpr < 8) wpr *= 2;
+  const int k8_per = (a.K / 8 + wpr - 1) / wpr;
+  for (int jw = warp; jw < a.R * wpr; jw += kRerankWarps) {
+    const int j = jw / wpr, part = jw - j * wpr;
     const int n = sel_id[j];
     float logit = -INFINITY;
     if (n >= 0 && n < a.N) {
       const uint4* wr = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(n) * a.K);
       const uint4* xr = reinterpret_cast<const uint4*>(xs);
       float acc = 0.0f;
-      for (int k8 = lane; k8 < a.K / 8; k8 += 32) {
+      const int k8_end = min(a.K / 8, (part + 1) * k8_per);
+      for (int k8 = part * k8_per + lane; k8 < k8_end; k8 += 32) {
         const uint4 w8 = wr[k8];
         const uint4 x8 = xr[k8];
         const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
@@ -158,10 +270,16 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
 #pragma unroll
       for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       logit = acc;
-    } else if (n >= a.N && lane == 0) {
+    } else if (n >= a.N && lane == 0 && part == 0) {
       set_status(a.status, DH_DEV_BAD_ID);
     }
-    if (lane == 0) sel_logit[j] = logit;
+    if (lane == 0) part_logit[jw] = logit;
+  }
+  __syncthreads();
+  for (int j = tid; j < a.R; j += kRerankThreads) {
+    float v = part_logit[j * wpr];
+    for (int q = 1; q < wpr; ++q) v += part_logit[j * wpr + q];
+    sel_logit[j] = v;
   }
   __syncthreads();
 
@@ -192,7 +310,8 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
 template <int LPT>
 static cudaError_t launch_rr(const RerankArgs& a, int M, cudaStream_t s) {
   size_t smem = static_cast<size_t>(2 * a.K) + sizeof(Sel) * (kRerankWarps + 1) +
-                static_cast<size_t>(a.R) * 8;
+                static_cast<size_t>(a.R) * 8 + static_cast<size_t>(a.R) * kRerankWarps * 4 +
+                sizeof(Sel) * kSurvivorCap + 4 * (kRerankWarps + 2);
   if (LPT == 0) smem += 4 * static_cast<size_t>((a.ncand + 31) / 32);
   cudaError_t e = cudaFuncSetAttribute(rerank_argmax_kernel<LPT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -238,16 +238,51 @@ class DraftHead:
         self.packed, self.S, self.ZS = quant(W, G)
         self.workspace = new_workspace(max_tokens, self.N, self.K, kcand, rerank, W.device)
         self.max_tokens = max_tokens
+        nblk = (self.N + BLOCK_ROWS - 1) // BLOCK_ROWS
+        dev = W.device
+        self._cv = torch.empty(max_tokens, nblk * kcand, dtype=torch.float32, device=dev)
+        self._ci = torch.empty(max_tokens, nblk * kcand, dtype=torch.int32, device=dev)
+        self._rr = torch.empty(max_tokens, rerank, dtype=torch.int32, device=dev)
+        self._rl = torch.empty(max_tokens, rerank, dtype=torch.float32, device=dev)
+        self._am = torch.empty(max_tokens, dtype=torch.int32, device=dev)
+
+    def infer(self, x_host: torch.Tensor, stream=None):
+        """End-to-end call from host memory: copies x_host (bf16 [M, K], pinned for an async
+        copy) to the device, runs the head, copies argmax [M], rr_id [M, R] and rr_logit [M, R]
+        back into pinned host tensors and synchronises the stream. Returns those host tensors."""
+        M = x_host.shape[0]
+        if not hasattr(self, "_x_dev") or self._x_dev.shape[0] < M:
+            dev = self.W.device
+            self._x_dev = torch.empty(self.max_tokens, self.K, dtype=torch.bfloat16, device=dev)
+            self._h_am = torch.empty(self.max_tokens, dtype=torch.int32, pin_memory=True)
+            self._h_rr = torch.empty(self.max_tokens, self.rerank, dtype=torch.int32,
+                                     pin_memory=True)
+            self._h_rl = torch.empty(self.max_tokens, self.rerank, dtype=torch.float32,
+                                     pin_memory=True)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        xd = self._x_dev[:M]
+        with torch.cuda.stream(s):
+            xd.copy_(_bf16(x_host, "x_host"), non_blocking=True)
+            out = self(xd, stream=s)
+            am, rr, rl = self._h_am[:M], self._h_rr[:M], self._h_rl[:M]
+            am.copy_(out["argmax"], non_blocking=True)
+            rr.copy_(out["rr_id"], non_blocking=True)
+            rl.copy_(out["rr_logit"], non_blocking=True)
+        s.synchronize()
+        return am, rr, rl
 
     def __call__(self, x: torch.Tensor, y_coarse=None, stream=None):
         """x bf16 [M, K] on the device -> dict of argmax [M], rr_id [M, R], rr_logit [M, R],
         cand_val, cand_id."""
         if x.shape[0] > self.max_tokens:
             raise ValueError(f"M={x.shape[0]} > max_tokens={self.max_tokens}")
+        M = x.shape[0]
         cv, ci = dh_draft_head_coarse_topk(x, self.packed, self.S, self.ZS, self.N, self.G,
-                                           self.bits, self.kcand, y_coarse=y_coarse,
+                                           self.bits, self.kcand, cand_val=self._cv[:M],
+                                           cand_id=self._ci[:M], y_coarse=y_coarse,
                                            workspace=self.workspace, stream=stream)
         rr, rl, am = dh_draft_head_rerank_argmax(x, self.W, cv, ci, self.rerank,
-                                                 y_coarse=y_coarse, workspace=self.workspace,
-                                                 stream=stream)
+                                                 rr_id=self._rr[:M], rr_logit=self._rl[:M],
+                                                 argmax_id=self._am[:M], y_coarse=y_coarse,
+                                                 workspace=self.workspace, stream=stream)
         return {"argmax": am, "rr_id": rr, "rr_logit": rl, "cand_val": cv, "cand_id": ci}

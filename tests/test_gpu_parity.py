@@ -65,6 +65,11 @@ COARSE_CASES = [
     (8, 2048, 2048, 64, 4, 8, 14),      # int4, G = 64 (fold per 64-byte sub-chunk)
     (2, 5120, 4096, 128, 2, 64, 15),    # K = 5120 (20 consumer warps), KCAND = 64
     (1, 1024, 70, 128, 2, 8, 16),       # two blocks, the second with 6 rows
+    # several 64-row blocks per CTA (partial buffers reused, jobs of many hidden rows)
+    (8, 5120, 58368, 128, 2, 8, 18),
+    (3, 2048, 58400, 64, 2, 4, 19),
+    (4, 5120, 124160, 128, 2, 8, 20),
+    (6, 2048, 30000, 128, 4, 2, 21),
 ]
 
 
