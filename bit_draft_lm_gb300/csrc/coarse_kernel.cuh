@@ -1,0 +1,528 @@
+// Coarse pass + block top-KCAND of the low-bit draft head (page "radiance_drafthead.py":
+// module docstring, _draft_head_int2 and _emit), for sm_103a.
+//
+// Work decomposition (GB300-first, not the page's one-program-per-block grid):
+//  * Persistent grid, one CTA per SM. A CTA walks 64-row candidate blocks b = blockIdx.x,
+//    blockIdx.x + gridDim.x, ...; each block is four 16-row tiles.
+//  * NW = K/256 warps. Warp w owns the same 256 k-values of every vocab row (its "strip": bytes
+//    [64w, 64w+64) of each int2 row, [128w, 128w+128) of each int4 row). So:
+//      - its share of the hidden states never changes: the x fragments of the MMA's B operand
+//        live in registers for the whole launch;
+//      - it streams only its own strip of each tile (16 rows x 64 B) through a private ring of
+//        shared-memory stages with 16-byte cp.async copies, NSW-1 tiles ahead: no warp waits for
+//        another warp's weights.
+//  * S and ZS of a block (64 contiguous rows each) arrive by two bulk (TMA) copies into a ring of
+//    block stages. The last warp to finish block b (an arrival counter) knows that every warp is
+//    done with b's stage and partials; it refills the stage with the S and ZS of the block that
+//    comes kSBlocks later and runs b's epilogue: it sums the NW partials in warp order
+//    (deterministic), selects the block's top-KCAND per hidden row with warp reductions (max
+//    key, lowest row on ties), writes the candidates and releases the partial buffer. No warp
+//    waits for that work; a warp waits only when it runs kSBlocks blocks ahead of the slowest
+//    warp (S stage) or nb blocks ahead of the epilogues (partial buffers).
+//  * Dequant in place, as f16 subnormals: in an f16 pair every bit of the low byte of each half
+//    is mantissa, so for a packed 32-bit word t (bytes b0..b3) the AND of t with the plane's
+//    code mask gives the f16 pair (b0's code, b2's code) * 2^(-24 + shift) exactly, and the
+//    same AND of t >> 8 gives (b1's code, b3's code): one LOP3 per MMA register (two weights),
+//    one shift per word. int2 planes 0..3 sit at bits 2p, 2p+1 (factor 2^(2p)); int4 nibbles at
+//    bits 0-3 and 4-7 (factor 2^(4p)). mma.sync m16n8k16 (f16 in, fp32 accumulate): weights on
+//    the 16-row side, hidden rows on the 8-column side; bytes j and j+2 of a word share an A
+//    register, and x is permuted the same way.
+//  * The hidden states enter the MMA's B operand as x * s / 2^shift in f16, with s a power of
+//    two per hidden row (max |x * s| in [2^14, 2^15)): exact for every element above the f16
+//    normal threshold, i.e. for all but those below max |x| * 2^-29 (error < 2^-25 scaled).
+//  * The page's dequant is 1 + v/L (L = 4 for int2, 16 for int4) on the group's S and ZS: a group
+//    contributes S * (XS + sum x v / L) - ZS * XS = (S - ZS) * XS + S * sum x v / L. With the MMA
+//    result D = s * 2^-24 * sum x v per (plane, group) of the strip, the warp accumulates
+//    acc = sum S * D - sum (ZS - S) * XS * s / kappa and the logit is y = (kappa / s) * acc, with
+//    kappa = 2^24 / L: powers of two, exact. Only one of the warps whose strips cover a group (its
+//    "owner") adds that group's zero-point term.
+//  * The per-group scale is applied to the accumulator, never to the weight tile.
+// Hidden rows are processed eight at a time (one MMA column tile); M > 8 runs ceil(M/8) passes.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "dh_device.cuh"
+#include "dh_launch.h"
+
+namespace dh {
+
+constexpr int kCoarseMaxWarps = 20;  // K <= 5120
+constexpr int kCoarseMaxThreads = kCoarseMaxWarps * 32;
+constexpr int kSBlocks = 4;     // S/ZS block stages
+constexpr int kMaxRedBufs = 4;  // partial buffers (blocks)
+
+struct CoarseArgs {
+  const uint16_t* x;  // bf16 [M, K]
+  int M, m0, mt;      // this pass covers hidden rows m0 .. m0+mt-1 (1 <= mt <= 8)
+  int K, N, G, KG, RB, NW;
+  const uint8_t* packed;  // [N, RB]
+  const uint16_t* S;      // [N, KG] bf16
+  const uint16_t* ZS;     // [N, KG] bf16
+  int kcand, nblk;
+  float* cand_val;  // [M, nblk*kcand]
+  int32_t* cand_id;
+  uint16_t* y;  // bf16 [M, N] or nullptr
+  uint32_t* status;
+  // 2^24 (t >> 8 as the high word of a product) and 2^16 (bf16 bits -> fp32): kernel parameters,
+  // so that these stay integer multiplies on the FMA pipe instead of shifts on the ALU pipe,
+  // which the dequant's ANDs keep busy.
+  uint32_t sh8_mul, u16_mul;
+  // shared-memory plan
+  int nb, red_pitch;
+  int off_bars, off_xs, off_sz, off_red, off_ring;
+};
+
+// 16-byte copy global -> shared (shared-space address); valid = false copies zeros.
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(gsrc),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u16(const unsigned char* p) {
+  return *reinterpret_cast<const uint16_t*>(p);
+}
+
+// Bounded wait by every lane of a warp (no warp collectives inside, so lanes may leave at
+// different moments). False if the wait ran out (then the launch is marked failed) or another
+// warp gave up first.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity,
+                                           volatile int* abort_flag, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(128);  // leave the issue slots to the warps that have work
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(status, DH_DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// f16 weights (two per register) of plane p from a packed word: code mask of the plane.
+template <int BITS>
+__device__ __forceinline__ uint32_t dq16(uint32_t t, int p) {
+  if (BITS == 2) return t & (0x00030003u << (2 * p));  // v * 2^(2p - 24)
+  return t & (0x000F000Fu << (4 * p));                 // v * 2^(4p - 24)
+}
+// log2 of the factor 2^shift of plane p's weights; the plane's x goes in divided by it.
+template <int BITS>
+__host__ __device__ constexpr int plane_shift(int p) {
+  return BITS == 2 ? 2 * p : 4 * p;
+}
+
+// G: the quantisation group (64 or 128). KSPEC: the hidden size K when it is known at compile
+// time (the vocabulary-scale head), 0 for a runtime K: with K fixed, every shared-memory offset
+// and stride below is an immediate. NSW: stages of each warp's private weight ring. MT1: a single
+// hidden row in this pass.
+template <int BITS, int G, int KSPEC, int NSW, bool MT1>
+__global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const CoarseArgs a) {
+  // SPLIT: the strip spans two quantisation groups per plane (int4 with G = 64), so the
+  // accumulator is folded once per 64-byte sub-chunk instead of once per strip.
+  // OWNHALF: a group spans the strips of two warps (int2 with G = 128); the warp whose parity is
+  // that of plane p owns plane p's zero-point term.
+  constexpr bool SPLIT = BITS == 4 && G == 64;
+  constexpr bool OWNHALF = BITS == 2 && G == 128;
+  constexpr int P = 8 / BITS;             // codes per byte (planes)
+  constexpr int SB = 256 / P;             // strip bytes per row: 256 k-values
+  constexpr int U = SB / 64;              // 64-byte sub-chunks per strip
+  constexpr int FS = SPLIT ? U : 1;       // fold segments per strip
+  constexpr int NQ = FS * P;              // scale groups per strip
+  constexpr int WSTAGE = kTileRows * SB;  // packed bytes of one warp's strip of a tile
+  constexpr int CH = WSTAGE / 16 / 32;    // 16-byte weight copies per lane per tile
+  constexpr int kLogL = BITS == 2 ? 2 : 4;  // log2 of the page's divisor L
+  static_assert((NSW & (NSW - 1)) == 0, "ring depth must be a power of two");
+  extern __shared__ __align__(128) unsigned char sm[];
+
+  const int K = KSPEC ? KSPEC : a.K;  // hidden size
+  const int NW = K / 256, KG = K / G, RB = K * BITS / 8;
+  const int mt = MT1 ? 1 : a.mt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int rp = MT1 ? 1 : a.red_pitch, nb = a.nb;
+  uint64_t* full_sb = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kSBlocks] S/ZS landed
+  uint64_t* red_empty = full_sb + kSBlocks;                            // [nb] partials consumed
+  int* blk_cnt = reinterpret_cast<int*>(red_empty + kMaxRedBufs);      // [nb] warps done
+  int* sz_issued = blk_cnt + kMaxRedBufs;                              // [kSBlocks] latest block
+  volatile int* abort_flag = sz_issued + kSBlocks;
+  float* xs_s = reinterpret_cast<float*>(sm + a.off_xs);  // [8][KG] group sums of x
+  int* xe_s = reinterpret_cast<int*>(xs_s + 8 * KG);      // [8] exponent E of max |x| per row
+  unsigned char* sz = sm + a.off_sz;                      // [kSBlocks][S|ZS][64][KG] bf16
+  float* red = reinterpret_cast<float*>(sm + a.off_red);  // [nb][NW][64][rp]
+  const int sz_half = kBlockRows * KG * 2;                // bytes of a stage's S (or ZS) rows
+  const int red_wstride = kBlockRows * rp;
+
+  const int my_blocks = (a.nblk - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                        static_cast<int>(gridDim.x);
+  const int my_tiles = my_blocks * kTilesPerBlock;
+  auto block_row0 = [&](int lb) {
+    return (static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x)) * kBlockRows;
+  };
+
+  // S and ZS rows of local block lb into stage lb % kSBlocks (rows past N are not copied; the
+  // epilogue ignores those rows). One thread.
+  auto issue_sz = [&](int lb) {
+    const int st = lb % kSBlocks;
+    const int row0 = block_row0(lb);
+    sz_issued[st] = lb;
+    int rows = a.N - row0;
+    rows = rows > kBlockRows ? kBlockRows : rows;
+    const uint32_t bytes = static_cast<uint32_t>(rows * KG * 2);  // multiple of 16: KG % 8 == 0
+    mbar_arrive_expect_tx(&full_sb[st], 2u * bytes);
+    unsigned char* dst = sz + st * 2 * sz_half;
+    bulk_g2s(dst, a.S + static_cast<int64_t>(row0) * KG, bytes, &full_sb[st]);
+    bulk_g2s(dst + sz_half, a.ZS + static_cast<int64_t>(row0) * KG, bytes, &full_sb[st]);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < kSBlocks; ++q) mbar_init(&full_sb[q], 1u);
+    for (int q = 0; q < kMaxRedBufs; ++q) {
+      mbar_init(&red_empty[q], 1u);
+      blk_cnt[q] = 0;
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+    for (int lb = 0; lb < kSBlocks && lb < my_blocks; ++lb) issue_sz(lb);
+  }
+
+  // ---- weight streaming of tile tau into ring stage tau % NSW, by warp `warp` alone:
+  // chunk e = lane + 32 j is row e / (SB/16), 16-byte column e % (SB/16) of the warp's strip;
+  // int4 rows are XOR-swizzled by (row & 1) so the two rows one quarter-warp reads use disjoint
+  // banks; rows past N are zero-filled.
+  const int strip_byte = warp * SB;
+  constexpr int CPR = SB / 16;   // 16-byte chunks per strip row
+  constexpr int RPJ = 32 / CPR;  // rows between a lane's successive chunks
+  const int r0l = lane / CPR, col0 = lane % CPR;
+  // the XOR swizzle depends on row parity only, and RPJ is even: the same for all of a lane's chunks
+  const int pcol0 = BITS == 4 ? (col0 ^ ((r0l & 1) << 2)) : col0;
+  const uint32_t dst_lane =
+      smem_addr(sm + a.off_ring + warp * (NSW * WSTAGE)) + r0l * SB + 16 * pcol0;
+  const int64_t src_lane = static_cast<int64_t>(r0l) * RB + strip_byte + 16 * col0;
+  const int64_t src_jstep = static_cast<int64_t>(RPJ) * RB;
+  auto load_tile = [&](int tau) {
+    if (tau < my_tiles) {
+      const int row0 = block_row0(tau >> 2) + (tau & 3) * kTileRows;
+      const uint8_t* src = a.packed + static_cast<int64_t>(row0) * RB + src_lane;
+      const uint32_t dst = dst_lane + (tau & (NSW - 1)) * WSTAGE;
+      if (row0 + kTileRows <= a.N) {
+#pragma unroll
+        for (int j = 0; j < CH; ++j) cp_async16(dst + j * RPJ * SB, src + j * src_jstep, true);
+      } else {
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+          const bool ok = row0 + r0l + j * RPJ < a.N;
+          cp_async16(dst + j * RPJ * SB, ok ? src + j * src_jstep : a.packed, ok);
+        }
+      }
+    }
+    cp_async_commit();  // one group per tile slot, possibly empty, keeps the counting uniform
+  };
+#pragma unroll
+  for (int t = 0; t < NSW - 1; ++t) load_tile(t);
+
+  // group sums of x in fp32 (the zero-point term) and the binary exponent of max |x| per row
+  for (int pr = warp; pr < mt * KG; pr += NW) {
+    const int tok = pr / KG, gi = pr - tok * KG;
+    const uint16_t* xr = a.x + static_cast<int64_t>(a.m0 + tok) * K + gi * G;
+    float sum = 0.0f;
+    for (int t = lane; t < G; t += 32) sum += bf16_bits_to_float(xr[t]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) xs_s[tok * KG + gi] = sum;
+  }
+  for (int tok = warp; tok < mt; tok += NW) {
+    const uint16_t* xr = a.x + static_cast<int64_t>(a.m0 + tok) * K;
+    uint32_t mx = 0;  // max of |x| as bf16 magnitude bits (monotone in the value)
+    for (int t = lane; t < K; t += 32) mx = max(mx, static_cast<uint32_t>(xr[t]) & 0x7fffu);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    // max = f * 2^E with f in [0.5, 1); E from the bf16 exponent field, clamped for zero/tiny rows
+    int E = static_cast<int>(mx >> 7) - 126;
+    E = E < -100 ? -100 : (E > 100 ? 100 : E);
+    if (lane == 0) xe_s[tok] = E;
+  }
+  __syncthreads();  // barriers initialised, group sums and scales complete
+
+  // S column of scale group q = (fold segment f, plane p) of this strip: p*(RB/G) + (strip+64f)/G
+  auto s_col = [&](int q) {
+    return (q % P) * (RB / G) + (strip_byte + 64 * (q / P)) / G;
+  };
+  auto pow2 = [](int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); };
+
+  // B operand: x of hidden row g for strip bytes 64u + 16c + 4i + {0, 2} (register 0) and
+  // {1, 3} (register 1), plane p, as f16 x * s / 2^plane_shift(p)
+  uint32_t bfr[U][4][P][2];
+  {
+    const bool valid = g < mt;
+    const int E = valid ? xe_s[g] : 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          uint32_t b0 = 0, b1 = 0;
+          if (valid) {
+            const int k0 = p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i;
+            const uint2 v = *reinterpret_cast<const uint2*>(
+                a.x + static_cast<int64_t>(a.m0 + g) * K + k0);
+            const float sx = pow2(15 - E - plane_shift<BITS>(p));  // max |x * s| in [2^14, 2^15)
+            const uint32_t h[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
+            uint32_t hs[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              hs[e] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(h[e]) * sx));
+            b0 = hs[0] | (hs[2] << 16);  // (x[k0], x[k0+2]): even bytes of the word
+            b1 = hs[1] | (hs[3] << 16);  // (x[k0+1], x[k0+3]): odd bytes
+          }
+          bfr[u][i][p][0] = b0;
+          bfr[u][i][p][1] = b1;
+        }
+  }
+
+  // byte offset of this lane's S entry of group (f, p) in a stage: so0 + p * pstride + 2 f
+  // (row g of tile t adds t * 16 rows; row g + 8 adds row8)
+  const int so0 = g * KG * 2 + 2 * s_col(0);
+  const int pstride = 2 * (RB / G);
+  const int row8 = 8 * KG * 2;
+  const unsigned char* ring = sm + a.off_ring + warp * (NSW * WSTAGE);
+  float* rw_base = red + warp * red_wstride + g * rp + 2 * c;
+
+  // ---- block epilogue: top-KCAND of every hidden row of local block lb, partials in buf
+  auto epilogue = [&](int lb, int buf) {
+    const int b = static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x);
+    const int n0 = b * kBlockRows + lane;
+    const float* rbuf = red + buf * NW * red_wstride;
+    for (int m = 0; m < mt; ++m) {
+      const float ysc = pow2(xe_s[m] + 9 - kLogL);  // kappa / s = 2^(24 - logL) * 2^(E - 15)
+      float v[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // fixed summation order (deterministic): four interleaved chains, then pairwise
+        const float* rb = rbuf + (lane + 32 * h) * rp + m;
+        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+        int w = 0;
+        for (; w + 4 <= NW; w += 4) {
+          s0 += rb[w * red_wstride];
+          s1 += rb[(w + 1) * red_wstride];
+          s2 += rb[(w + 2) * red_wstride];
+          s3 += rb[(w + 3) * red_wstride];
+        }
+        for (; w < NW; ++w) s0 += rb[w * red_wstride];
+        v[h] = ((s0 + s1) + (s2 + s3)) * ysc;
+      }
+      if (a.y) {
+        uint16_t* yr = a.y + static_cast<int64_t>(a.m0 + m) * a.N;
+        if (n0 < a.N) yr[n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
+        if (n0 + 32 < a.N) yr[n0 + 32] = __bfloat16_as_ushort(__float2bfloat16_rn(v[1]));
+      }
+      uint32_t k0 = n0 < a.N ? order_key(v[0]) : 0u;
+      uint32_t k1 = n0 + 32 < a.N ? order_key(v[1]) : 0u;
+      uint32_t key_lo = 0u, row_lo = 64u, key_hi = 0u, row_hi = 64u;  // slots lane, lane + 32
+      for (int r = 0; r < a.kcand; ++r) {
+        const bool first = k0 >= k1;
+        const uint32_t bk = first ? k0 : k1;
+        const uint32_t brow = first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t rwin = __reduce_min_sync(0xffffffffu, bk == kmax ? brow : 64u);
+        if (kmax != 0u && lane == static_cast<int>(rwin & 31u)) {
+          if (rwin < 32u) k0 = 0u; else k1 = 0u;
+        }
+        if (lane == (r & 31)) {
+          if (r < 32) {
+            key_lo = kmax;
+            row_lo = kmax ? rwin : 64u;
+          } else {
+            key_hi = kmax;
+            row_hi = kmax ? rwin : 64u;
+          }
+        }
+      }
+      const int64_t obase = static_cast<int64_t>(a.m0 + m) * a.nblk * a.kcand +
+                            static_cast<int64_t>(b) * a.kcand;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int slot = lane + 32 * h;
+        const uint32_t kk = h ? key_hi : key_lo, rr = h ? row_hi : row_lo;
+        if (slot < a.kcand) {
+          a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
+          a.cand_id[obase + slot] = kk ? b * kBlockRows + static_cast<int>(rr) : -1;
+        }
+      }
+    }
+  };
+
+  auto run = [&](auto par_tag) {
+    constexpr int PAR = decltype(par_tag)::value;
+    // zero-point weights of the lane's accumulator columns (hidden rows 2c, 2c + 1) for each
+    // group the warp owns: XS * s / kappa = XS * 2^(15 - E) * 2^(logL - 24)
+    float xsv[NQ][2];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int hr = 2 * c + j;
+        xsv[q][j] = (!OWNHALF || ((q % P) & 1) == PAR) && hr < mt
+                        ? xs_s[hr * KG + s_col(q)] * pow2(kLogL - 9 - xe_s[hr])
+                        : 0.0f;
+      }
+    for (int tau = 0; tau < my_tiles; ++tau) {
+      load_tile(tau + NSW - 1);  // into the stage the previous tile freed
+      cp_async_wait<NSW - 1>();  // tile tau has landed (for this lane's copies)
+      __syncwarp();              // ... and for every lane's
+      const int t = tau & 3, lb = tau >> 2, buf = lb & (nb - 1);
+      const int sst = lb % kSBlocks;
+      if (t == 0) {
+        bool ok = wait_phase(&full_sb[sst], static_cast<uint32_t>(lb / kSBlocks) & 1u, abort_flag,
+                             a.status);
+        if (lb >= nb)
+          ok = wait_phase(&red_empty[buf], static_cast<uint32_t>(lb / nb - 1) & 1u, abort_flag,
+                          a.status) &&
+               ok;
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+
+      const unsigned char* cs = ring + (tau & (NSW - 1)) * WSTAGE;  // this warp's stage
+      const unsigned char* szs = sz + sst * 2 * sz_half + t * (kTileRows * KG * 2) + so0;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float d[P][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int pc = BITS == 4 ? ((4 * u + c) ^ ((g & 1) << 2)) : c;  // swizzled column
+        const uint4 wa = *reinterpret_cast<const uint4*>(cs + g * SB + 16 * pc);
+        const uint4 wb = *reinterpret_cast<const uint4*>(cs + (g + 8) * SB + 16 * pc);
+        const uint32_t ta[4] = {wa.x, wa.y, wa.z, wa.w}, tb[4] = {wb.x, wb.y, wb.z, wb.w};
+        uint32_t tao[4], tbo[4];  // odd bytes moved down: t >> 8 (the multiply's high word)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tao[i] = __umulhi(ta[i], a.sh8_mul);
+          tbo[i] = __umulhi(tb[i], a.sh8_mul);
+        }
+        const int f = SPLIT ? u : 0;
+        const bool seg_first = SPLIT || u == 0, seg_last = SPLIT || u == U - 1;
+        // plane by plane: the plane's accumulator is folded as soon as its segment is complete
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          if (seg_first) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[p][e] = 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mma_f16_16816_acc(d[p], dq16<BITS>(ta[i], p), dq16<BITS>(tb[i], p),
+                              dq16<BITS>(tao[i], p), dq16<BITS>(tbo[i], p), bfr[u][i][p][0],
+                              bfr[u][i][p][1]);
+          if (seg_last) {
+            // fold: acc += S * D; the owner subtracts (ZS - S) * XS * s / kappa
+            const int q = f * P + p;
+            const unsigned char* sq = szs + p * pstride + 2 * f;
+            const float sg = __uint_as_float(lds_u16(sq) * a.u16_mul);
+            const float sg8 = __uint_as_float(lds_u16(sq + row8) * a.u16_mul);
+            acc[0] = fmaf(sg, d[p][0], acc[0]);
+            acc[1] = fmaf(sg, d[p][1], acc[1]);
+            acc[2] = fmaf(sg8, d[p][2], acc[2]);
+            acc[3] = fmaf(sg8, d[p][3], acc[3]);
+            if (!OWNHALF || (p & 1) == PAR) {
+              const float zc = __uint_as_float(lds_u16(sq + sz_half) * a.u16_mul) - sg;
+              const float zc8 = __uint_as_float(lds_u16(sq + sz_half + row8) * a.u16_mul) - sg8;
+              acc[0] = fmaf(-zc, xsv[q][0], acc[0]);
+              acc[1] = fmaf(-zc, xsv[q][1], acc[1]);
+              acc[2] = fmaf(-zc8, xsv[q][0], acc[2]);
+              acc[3] = fmaf(-zc8, xsv[q][1], acc[3]);
+            }
+          }
+        }
+      }
+      // partials, D layout: acc[0..1] = row g, hidden rows 2c, 2c+1; acc[2..3] = row g + 8
+      float* rw = rw_base + (buf * NW * kBlockRows + t * kTileRows) * rp;
+      if (2 * c < mt) {
+        rw[0] = acc[0];
+        rw[8 * rp] = acc[2];
+      }
+      if (2 * c + 1 < mt) {
+        rw[1] = acc[1];
+        rw[8 * rp + 1] = acc[3];
+      }
+      if (t == kTilesPerBlock - 1) {
+        // end of block lb for this warp; the last warp to get here finishes the block
+        __syncwarp();  // every lane's partial stores and stage reads are done
+        int last = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          last = atomicAdd(&blk_cnt[buf], 1) == NW - 1;
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence_block();  // the other warps' partials are visible to every lane
+          if (lane == 0) {
+            blk_cnt[buf] = 0;
+            if (lb + kSBlocks < my_blocks) {
+              fence_proxy_async_smem();  // stage reads above happen before the copy's writes
+              issue_sz(lb + kSBlocks);
+            }
+          }
+          epilogue(lb, buf);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&red_empty[buf]);
+        }
+      }
+    }
+  };
+  if (OWNHALF && (warp & 1))
+    run(std::integral_constant<int, 1>{});
+  else
+    run(std::integral_constant<int, 0>{});
+  cp_async_wait<0>();
+  // After an abort, S/ZS copies may still be in flight: they must land before the CTA's shared
+  // memory goes away. (Normally every issued stage has been waited for already.)
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int q = 0; q < kSBlocks && q < my_blocks; ++q)
+      mbar_wait_bounded(&full_sb[q], static_cast<uint32_t>(sz_issued[q] / kSBlocks) & 1u);
+  }
+}
+
+
+// Launches one pass (hidden rows m0 .. m0 + mt - 1) of the kernel for a given plan: the hidden
+// size is compiled in for K = 5120, the single-row case for mt = 1.
+template <int BITS, int G>
+cudaError_t launch_coarse_variant(const CoarseArgs& a, int nsw, int grid, cudaStream_t s) {
+  auto go = [&](auto kernel) -> cudaError_t {
+    constexpr int SB = BITS == 2 ? 64 : 128;
+    const int smem = a.off_ring + a.NW * nsw * kTileRows * SB;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, a.NW * 32, smem, s>>>(a);
+    return cudaGetLastError();
+  };
+  auto by_nsw = [&](auto kspec, auto mt1) -> cudaError_t {
+    constexpr int KS = decltype(kspec)::value;
+    constexpr bool M1 = decltype(mt1)::value;
+    switch (nsw) {
+      case 8: return go(coarse_topk_kernel<BITS, G, KS, 8, M1>);
+      case 4: return go(coarse_topk_kernel<BITS, G, KS, 4, M1>);
+      default: return go(coarse_topk_kernel<BITS, G, KS, 2, M1>);
+    }
+  };
+  using K0 = std::integral_constant<int, 0>;
+  using K5120 = std::integral_constant<int, 5120>;
+  using T = std::true_type;
+  using F = std::false_type;
+  if (a.K == 5120) return a.mt == 1 ? by_nsw(K5120{}, T{}) : by_nsw(K5120{}, F{});
+  return a.mt == 1 ? by_nsw(K0{}, T{}) : by_nsw(K0{}, F{});
+}
+
+}  // namespace dh
