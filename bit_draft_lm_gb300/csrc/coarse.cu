@@ -23,9 +23,9 @@ static int plan_coarse(CoarseArgs& a, int max_smem, int nsw_max) {
   a.red_pitch = mt_max | 1;  // odd: a warp reading one column over 32 rows hits 32 banks
   int off = 0;
   a.off_bars = off;
-  off += (kSBlocks + kMaxRedBufs) * 8 + (kMaxRedBufs + kSBlocks) * 4 + 16;
+  off += (kSBlocks + kMaxRedBufs) * 8 + (3 * kMaxRedBufs + kSBlocks + 2) * 4 + 16;
   a.off_xs = off = (off + 15) / 16 * 16;
-  off += 8 * a.KG * 4 + 8 * 4;
+  off += a.NW * 8 * 4 * 4;  // strip group sums: [NW][8 rows][<= 4 groups] fp32
   a.off_sz = off = (off + 127) / 128 * 128;
   off += kSBlocks * 2 * kBlockRows * a.KG * 2;
   a.off_red = off = (off + 15) / 16 * 16;

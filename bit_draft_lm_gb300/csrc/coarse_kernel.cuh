@@ -14,11 +14,12 @@
 //  * S and ZS of a block (64 contiguous rows each) arrive by two bulk (TMA) copies into a ring of
 //    block stages. The last warp to finish block b (an arrival counter) knows that every warp is
 //    done with b's stage and partials; it refills the stage with the S and ZS of the block that
-//    comes kSBlocks later and runs b's epilogue: it sums the NW partials in warp order
-//    (deterministic), selects the block's top-KCAND per hidden row with warp reductions (max
-//    key, lowest row on ties), writes the candidates and releases the partial buffer. No warp
-//    waits for that work; a warp waits only when it runs kSBlocks blocks ahead of the slowest
-//    warp (S stage) or nb blocks ahead of the epilogues (partial buffers).
+//    comes kSBlocks later and publishes b's epilogue as one job per hidden row. Warps claim jobs
+//    at block boundaries and while they wait (so the fastest warps do them, in parallel): a job
+//    sums the NW partials of its rows in a fixed order (deterministic), selects the top-KCAND
+//    with warp reductions (max key, lowest row on ties) and writes the candidates; the block's
+//    last job releases its partial buffer. A warp waits only when it runs kSBlocks blocks ahead
+//    of the slowest warp (S stage) or nb blocks ahead of the epilogues (partial buffers).
 //  * Dequant in place, as f16 subnormals: in an f16 pair every bit of the low byte of each half
 //    is mantissa, so for a packed 32-bit word t (bytes b0..b3) the AND of t with the plane's
 //    code mask gives the f16 pair (b0's code, b2's code) * 2^(-24 + shift) exactly, and the
@@ -95,25 +96,6 @@ __device__ __forceinline__ uint32_t lds_u16(const unsigned char* p) {
   return *reinterpret_cast<const uint16_t*>(p);
 }
 
-// Bounded wait by every lane of a warp (no warp collectives inside, so lanes may leave at
-// different moments). False if the wait ran out (then the launch is marked failed) or another
-// warp gave up first.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity,
-                                           volatile int* abort_flag, uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    __nanosleep(128);  // leave the issue slots to the warps that have work
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      set_status(status, DH_DEV_WAIT_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 // f16 weights (two per register) of plane p from a packed word: code mask of the plane.
 template <int BITS>
 __device__ __forceinline__ uint32_t dq16(uint32_t t, int p) {
@@ -159,9 +141,12 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   uint64_t* red_empty = full_sb + kSBlocks;                            // [nb] partials consumed
   int* blk_cnt = reinterpret_cast<int*>(red_empty + kMaxRedBufs);      // [nb] warps done
   int* sz_issued = blk_cnt + kMaxRedBufs;                              // [kSBlocks] latest block
-  volatile int* abort_flag = sz_issued + kSBlocks;
-  float* xs_s = reinterpret_cast<float*>(sm + a.off_xs);  // [8][KG] group sums of x
-  int* xe_s = reinterpret_cast<int*>(xs_s + 8 * KG);      // [8] exponent E of max |x| per row
+  int* job_done = sz_issued + kSBlocks;      // [nb] epilogue jobs finished per partial buffer
+  int* job_pub = job_done + kMaxRedBufs;     // [nb] warp that published the buffer's jobs
+  int* jobs_ready = job_pub + kMaxRedBufs;   // jobs [0, jobs_ready) may run
+  int* jobs_claimed = jobs_ready + 1;        // jobs [0, jobs_claimed) taken by some warp
+  volatile int* abort_flag = jobs_claimed + 1;
+  float* xs_half = reinterpret_cast<float*>(sm + a.off_xs);  // [NW][8][NQ] strip group sums
   unsigned char* sz = sm + a.off_sz;                      // [kSBlocks][S|ZS][64][KG] bf16
   float* red = reinterpret_cast<float*>(sm + a.off_red);  // [nb][NW][64][rp]
   const int sz_half = kBlockRows * KG * 2;                // bytes of a stage's S (or ZS) rows
@@ -195,6 +180,9 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
       mbar_init(&red_empty[q], 1u);
       blk_cnt[q] = 0;
     }
+    for (int q = 0; q < kMaxRedBufs; ++q) job_done[q] = job_pub[q] = 0;
+    *jobs_ready = 0;
+    *jobs_claimed = 0;
     *abort_flag = 0;
     mbar_fence_init();
     for (int lb = 0; lb < kSBlocks && lb < my_blocks; ++lb) issue_sz(lb);
@@ -232,30 +220,22 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     }
     cp_async_commit();  // one group per tile slot, possibly empty, keeps the counting uniform
   };
+  // ---- this warp's view of x (hidden row g, lanes g < mt), loaded before the weight prefetch so
+  // that it does not queue behind it: the strip's values for the MMA's B operand.
+  const uint16_t* xg = a.x + static_cast<int64_t>(a.m0 + (g < mt ? g : 0)) * K;  // hidden row g
+  uint2 xv[U][4][P];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int p = 0; p < P; ++p)
+        xv[u][i][p] = g < mt ? *reinterpret_cast<const uint2*>(
+                                   xg + p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i)
+                             : make_uint2(0u, 0u);
+
 #pragma unroll
   for (int t = 0; t < NSW - 1; ++t) load_tile(t);
-
-  // group sums of x in fp32 (the zero-point term) and the binary exponent of max |x| per row
-  for (int pr = warp; pr < mt * KG; pr += NW) {
-    const int tok = pr / KG, gi = pr - tok * KG;
-    const uint16_t* xr = a.x + static_cast<int64_t>(a.m0 + tok) * K + gi * G;
-    float sum = 0.0f;
-    for (int t = lane; t < G; t += 32) sum += bf16_bits_to_float(xr[t]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) xs_s[tok * KG + gi] = sum;
-  }
-  for (int tok = warp; tok < mt; tok += NW) {
-    const uint16_t* xr = a.x + static_cast<int64_t>(a.m0 + tok) * K;
-    uint32_t mx = 0;  // max of |x| as bf16 magnitude bits (monotone in the value)
-    for (int t = lane; t < K; t += 32) mx = max(mx, static_cast<uint32_t>(xr[t]) & 0x7fffu);
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    // max = f * 2^E with f in [0.5, 1); E from the bf16 exponent field, clamped for zero/tiny rows
-    int E = static_cast<int>(mx >> 7) - 126;
-    E = E < -100 ? -100 : (E > 100 ? 100 : E);
-    if (lane == 0) xe_s[tok] = E;
-  }
-  __syncthreads();  // barriers initialised, group sums and scales complete
 
   // S column of scale group q = (fold segment f, plane p) of this strip: p*(RB/G) + (strip+64f)/G
   auto s_col = [&](int q) {
@@ -264,35 +244,69 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   auto pow2 = [](int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); };
 
   // B operand: x of hidden row g for strip bytes 64u + 16c + 4i + {0, 2} (register 0) and
-  // {1, 3} (register 1), plane p, as f16 x * s / 2^plane_shift(p)
+  // {1, 3} (register 1), plane p, as f16 x * s / 2^plane_shift(p). Each warp scales by its own
+  // power of two s = 2^(15 - E), max |x| = f * 2^E (f in [0.5, 1)) over its strip of the row,
+  // and converts its partials to logit units before storing them. Also the sums of x over the
+  // strip's part of each scale group q (the zero-point term).
   uint32_t bfr[U][4][P][2];
+  int ew;  // E of this warp's strip of hidden row g
+  float xsg[NQ];
   {
-    const bool valid = g < mt;
-    const int E = valid ? xe_s[g] : 0;
+    uint32_t mx = 0;  // max |x| as bf16 magnitude bits (monotone in the value)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) xsg[q] = 0.0f;
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-          uint32_t b0 = 0, b1 = 0;
-          if (valid) {
-            const int k0 = p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i;
-            const uint2 v = *reinterpret_cast<const uint2*>(
-                a.x + static_cast<int64_t>(a.m0 + g) * K + k0);
-            const float sx = pow2(15 - E - plane_shift<BITS>(p));  // max |x * s| in [2^14, 2^15)
-            const uint32_t h[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
-            uint32_t hs[4];
+          const uint2 v = xv[u][i][p];
+          mx = max(mx, max(max(v.x & 0x7fffu, (v.x >> 16) & 0x7fffu),
+                           max(v.y & 0x7fffu, (v.y >> 16) & 0x7fffu)));
+          xsg[(SPLIT ? u : 0) * P + p] += (bf16_bits_to_float(v.x & 0xffffu) + bf16_bits_to_float(v.x >> 16)) +
+                                          (bf16_bits_to_float(v.y & 0xffffu) + bf16_bits_to_float(v.y >> 16));
+        }
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));  // the row's four lanes
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              hs[e] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(h[e]) * sx));
-            b0 = hs[0] | (hs[2] << 16);  // (x[k0], x[k0+2]): even bytes of the word
-            b1 = hs[1] | (hs[3] << 16);  // (x[k0+1], x[k0+3]): odd bytes
-          }
-          bfr[u][i][p][0] = b0;
-          bfr[u][i][p][1] = b1;
+    for (int q = 0; q < NQ; ++q) {
+      xsg[q] += __shfl_xor_sync(0xffffffffu, xsg[q], 1);
+      xsg[q] += __shfl_xor_sync(0xffffffffu, xsg[q], 2);
+    }
+    ew = static_cast<int>(mx >> 7) - 126;
+    ew = ew < -100 ? -100 : (ew > 100 ? 100 : ew);  // zero or tiny rows
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          const float sx = pow2(15 - ew - plane_shift<BITS>(p));  // max |x * s| < 2^15
+          const uint2 v = xv[u][i][p];
+          const uint32_t h[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
+          uint32_t hs[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            hs[e] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(h[e]) * sx));
+          bfr[u][i][p][0] = hs[0] | (hs[2] << 16);  // (x[k0], x[k0+2]): even bytes of the word
+          bfr[u][i][p][1] = hs[1] | (hs[3] << 16);  // (x[k0+1], x[k0+3]): odd bytes
         }
   }
+  // A group of 128 int2 k-values spans the strips of warps 2j, 2j+1: the halves meet in shared
+  // memory (lower warp's half first, a fixed order).
+  if (OWNHALF && c == 0) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) xs_half[(warp * 8 + g) * NQ + q] = xsg[q];
+  }
+  __syncthreads();  // barriers initialised, strip sums published
+  if (OWNHALF) {
+    const int w0 = warp & ~1;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      xsg[q] = xs_half[(w0 * 8 + g) * NQ + q] + xs_half[((w0 + 1) * 8 + g) * NQ + q];
+  }
+
 
   // byte offset of this lane's S entry of group (f, p) in a stage: so0 + p * pstride + 2 f
   // (row g of tile t adds t * 16 rows; row g + 8 adds row8)
@@ -302,13 +316,12 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   const unsigned char* ring = sm + a.off_ring + warp * (NSW * WSTAGE);
   float* rw_base = red + warp * red_wstride + g * rp + 2 * c;
 
-  // ---- block epilogue: top-KCAND of every hidden row of local block lb, partials in buf
-  auto epilogue = [&](int lb, int buf) {
+  // ---- epilogue job: top-KCAND of hidden row m of local block lb, partials in buf
+  auto epilogue = [&](int lb, int buf, int m) {
     const int b = static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x);
     const int n0 = b * kBlockRows + lane;
     const float* rbuf = red + buf * NW * red_wstride;
-    for (int m = 0; m < mt; ++m) {
-      const float ysc = pow2(xe_s[m] + 9 - kLogL);  // kappa / s = 2^(24 - logL) * 2^(E - 15)
+    {
       float v[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
           s3 += rb[(w + 3) * red_wstride];
         }
         for (; w < NW; ++w) s0 += rb[w * red_wstride];
-        v[h] = ((s0 + s1) + (s2 + s3)) * ysc;
+        v[h] = (s0 + s1) + (s2 + s3);
       }
       if (a.y) {
         uint16_t* yr = a.y + static_cast<int64_t>(a.m0 + m) * a.N;
@@ -366,20 +379,77 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     }
   };
 
+  // ---- epilogue jobs: job j = lb * mt + m is hidden row m of local block lb; it may run once
+  // jobs_ready > j (block lb complete). Every decision is lane 0's, broadcast, so that all lanes
+  // take the same path (the epilogue holds warp-wide reductions).
+  // own = false: leave jobs this warp published itself (it finished the block last: it is the
+  // slowest warp) to the others.
+  auto try_job = [&](bool own) -> bool {
+    int j = -1;
+    if (lane == 0) {
+      const int cl = *reinterpret_cast<volatile int*>(jobs_claimed);
+      if (cl < *reinterpret_cast<volatile int*>(jobs_ready) &&
+          (own || *reinterpret_cast<volatile int*>(&job_pub[(MT1 ? cl : cl / mt) & (nb - 1)]) != warp) &&
+          atomicCAS(jobs_claimed, cl, cl + 1) == cl)
+        j = cl;
+    }
+    j = __shfl_sync(0xffffffffu, j, 0);
+    if (j < 0) return false;
+    const int jb = MT1 ? j : j / mt, m = MT1 ? 0 : j - jb * mt, jbuf = jb & (nb - 1);
+    __syncwarp();
+    __threadfence_block();  // the block's partials, published before jobs_ready, are visible
+    epilogue(jb, jbuf, m);
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (MT1 || atomicAdd(&job_done[jbuf], 1) == mt - 1) {  // the block's last job
+        if (!MT1) job_done[jbuf] = 0;
+        mbar_arrive(&red_empty[jbuf]);
+      }
+    }
+    return true;
+  };
+  // Bounded wait for phase `parity` of `bar`: runs an epilogue job if one is ready, else lane 0
+  // sleeps in the mbarrier (woken when the phase completes, or after a few microseconds to look
+  // for jobs again). False after a timeout (the launch is marked failed) or another warp's.
+  auto wait_taking_jobs = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      int st = 0;
+      if (lane == 0) st = mbar_test_wait(bar, parity) ? 1 : (*abort_flag ? -1 : 0);
+      st = __shfl_sync(0xffffffffu, st, 0);
+      if (st > 0) {
+        mbar_test_wait(bar, parity);  // every lane acquires (the phase stays complete)
+        return true;
+      }
+      if (st < 0) return false;
+      if (try_job(true)) continue;
+      if (lane == 0) mbar_try_wait_ns(bar, parity, 4000u);
+      __syncwarp();
+      if (lane == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        set_status(a.status, DH_DEV_WAIT_TIMEOUT);
+      }
+    }
+  };
+
   auto run = [&](auto par_tag) {
     constexpr int PAR = decltype(par_tag)::value;
-    // zero-point weights of the lane's accumulator columns (hidden rows 2c, 2c + 1) for each
-    // group the warp owns: XS * s / kappa = XS * 2^(15 - E) * 2^(logL - 24)
-    float xsv[NQ][2];
+    // For the lane's accumulator columns (hidden rows 2c, 2c + 1): the zero-point weights
+    // XS * s / kappa = XS * 2^(15 - E) * 2^(logL - 24) of the owned groups, and the factor
+    // kappa / s that turns the partials into logits.
+    float xsv[NQ][2], ysc[2];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q)
+    for (int j = 0; j < 2; ++j) {
+      const int hr = 2 * c + j, src = (hr < 8 ? hr : 0) * 4;
+      const int e = __shfl_sync(0xffffffffu, ew, src);
+      ysc[j] = hr < mt ? pow2(e + 9 - kLogL) : 0.0f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int hr = 2 * c + j;
-        xsv[q][j] = (!OWNHALF || ((q % P) & 1) == PAR) && hr < mt
-                        ? xs_s[hr * KG + s_col(q)] * pow2(kLogL - 9 - xe_s[hr])
-                        : 0.0f;
+      for (int q = 0; q < NQ; ++q) {
+        const float xs = __shfl_sync(0xffffffffu, xsg[q], src);
+        xsv[q][j] = (!OWNHALF || ((q % P) & 1) == PAR) && hr < mt ? xs * pow2(kLogL - 9 - e) : 0.0f;
       }
+    }
     for (int tau = 0; tau < my_tiles; ++tau) {
       load_tile(tau + NSW - 1);  // into the stage the previous tile freed
       cp_async_wait<NSW - 1>();  // tile tau has landed (for this lane's copies)
@@ -387,13 +457,11 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
       const int t = tau & 3, lb = tau >> 2, buf = lb & (nb - 1);
       const int sst = lb % kSBlocks;
       if (t == 0) {
-        bool ok = wait_phase(&full_sb[sst], static_cast<uint32_t>(lb / kSBlocks) & 1u, abort_flag,
-                             a.status);
-        if (lb >= nb)
-          ok = wait_phase(&red_empty[buf], static_cast<uint32_t>(lb / nb - 1) & 1u, abort_flag,
-                          a.status) &&
-               ok;
-        if (!__all_sync(0xffffffffu, ok)) break;
+        bool ok = wait_taking_jobs(&full_sb[sst], static_cast<uint32_t>(lb / kSBlocks) & 1u);
+        if (ok && lb >= nb)
+          ok = wait_taking_jobs(&red_empty[buf], static_cast<uint32_t>(lb / nb - 1) & 1u);
+        if (!ok) break;
+        try_job(false);  // an epilogue another warp published, if one is ready
       }
 
       const unsigned char* cs = ring + (tau & (NSW - 1)) * WSTAGE;  // this warp's stage
@@ -450,34 +518,45 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
       // partials, D layout: acc[0..1] = row g, hidden rows 2c, 2c+1; acc[2..3] = row g + 8
       float* rw = rw_base + (buf * NW * kBlockRows + t * kTileRows) * rp;
       if (2 * c < mt) {
-        rw[0] = acc[0];
-        rw[8 * rp] = acc[2];
+        rw[0] = acc[0] * ysc[0];
+        rw[8 * rp] = acc[2] * ysc[0];
       }
       if (2 * c + 1 < mt) {
-        rw[1] = acc[1];
-        rw[8 * rp + 1] = acc[3];
+        rw[1] = acc[1] * ysc[1];
+        rw[8 * rp + 1] = acc[3] * ysc[1];
       }
       if (t == kTilesPerBlock - 1) {
-        // end of block lb for this warp; the last warp to get here finishes the block
+        // end of block lb for this warp. The last warp to get here refills the block's S/ZS
+        // stage and publishes the block's epilogue jobs.
         __syncwarp();  // every lane's partial stores and stage reads are done
-        int last = 0;
         if (lane == 0) {
           __threadfence_block();
-          last = atomicAdd(&blk_cnt[buf], 1) == NW - 1;
-        }
-        if (__shfl_sync(0xffffffffu, last, 0)) {
-          __threadfence_block();  // the other warps' partials are visible to every lane
-          if (lane == 0) {
+          if (atomicAdd(&blk_cnt[buf], 1) == NW - 1) {
             blk_cnt[buf] = 0;
+            __threadfence_block();
             if (lb + kSBlocks < my_blocks) {
-              fence_proxy_async_smem();  // stage reads above happen before the copy's writes
+              fence_proxy_async_smem();  // stage reads happen before the copy's writes
               issue_sz(lb + kSBlocks);
             }
+            job_pub[buf] = warp;
+            __threadfence_block();
+            atomicMax(jobs_ready, (lb + 1) * mt);
           }
-          epilogue(lb, buf);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&red_empty[buf]);
         }
+      }
+    }
+    // drain: take epilogue jobs until every job of this CTA has been taken by some warp
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      int st = 0;
+      if (lane == 0)
+        st = *reinterpret_cast<volatile int*>(jobs_claimed) >= my_blocks * mt || *abort_flag;
+      if (__shfl_sync(0xffffffffu, st, 0)) break;
+      if (try_job(true)) continue;
+      __nanosleep(128);
+      if (lane == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        set_status(a.status, DH_DEV_WAIT_TIMEOUT);
       }
     }
   };
