@@ -60,9 +60,15 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+COARSE_SOURCES = ("coarse.cu", "coarse_kernel.cuh", "coarse_i2g128.cu", "coarse_i2g64.cu",
+                  "coarse_i4g128.cu", "coarse_i4g64.cu", "dh_device.cuh")
+
+
 def coarse_source_hash():
+    """Fingerprint of the coarse kernel's sources: a profiled traffic figure is used only while
+    it still describes the kernel being timed."""
     h = hashlib.sha256()
-    for f in ("coarse.cu", "dh_device.cuh"):
+    for f in COARSE_SOURCES:
         with open(os.path.join(ROOT, "bit_draft_lm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
