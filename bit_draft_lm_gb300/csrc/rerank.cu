@@ -83,6 +83,16 @@ __device__ __forceinline__ Sel warp_sort(Sel v) {
 }
 
 constexpr int kSurvivorCap = 256;  // candidates the one-warp exact selection takes after the filter
+constexpr int kRerankUnroll = 8;   // weight-row loads each lane keeps in flight
+
+// 16-byte load through the read-only (non-coherent) path: W is never written by the library.
+__device__ __forceinline__ uint4 ldg_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}  // candidates the one-warp exact selection takes after the filter
 
 template <int LPT>
 __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const RerankArgs a) {
@@ -100,8 +110,6 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
   const int m = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint16_t* xrow = a.x + static_cast<int64_t>(m) * a.K;
-  for (int i = tid; i < a.K / 8; i += kRerankThreads)
-    reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(xrow)[i];
 
   const float* cv = a.cand_val + static_cast<int64_t>(m) * a.ncand;
   const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
@@ -119,6 +127,10 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
     const int i = tid + j * kRerankThreads;
     key[j] = i < a.ncand ? order_key(cv[i]) : 0u;
   }
+
+  // the hidden row, staged for the rerank dots (its loads overlap those of the keys)
+  for (int i = tid; i < a.K / 8; i += kRerankThreads)
+    reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(xrow)[i];
 
   // Fast exact path. T = the R-th largest of the 32 warp maxima is at most the R-th largest
   // candidate (those R maxima are R distinct candidates >= T), so every member of the top R has
@@ -253,19 +265,31 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
       const uint4* xr = reinterpret_cast<const uint4*>(xs);
       float acc = 0.0f;
       const int k8_end = min(a.K / 8, (part + 1) * k8_per);
-      for (int k8 = part * k8_per + lane; k8 < k8_end; k8 += 32) {
-        const uint4 w8 = wr[k8];
-        const uint4 x8 = xr[k8];
-        const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
-        const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
-        float part = 0.0f;
+      // kRerankUnroll 16-byte loads of the weight row in flight per lane before any is used
+      for (int k8b = part * k8_per + lane; k8b < k8_end; k8b += 32 * kRerankUnroll) {
+        uint4 w8[kRerankUnroll];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          part = fmaf(__uint_as_float(xv[q] << 16), __uint_as_float(wv[q] << 16), part);
-          part = fmaf(__uint_as_float(xv[q] & 0xffff0000u), __uint_as_float(wv[q] & 0xffff0000u),
-                      part);
+        for (int u = 0; u < kRerankUnroll; ++u) {
+          const int k8 = k8b + 32 * u;
+          w8[u] = k8 < k8_end ? ldg_nc_v4(wr + k8) : make_uint4(0u, 0u, 0u, 0u);
         }
-        acc += part;
+#pragma unroll
+        for (int u = 0; u < kRerankUnroll; ++u) {
+          const int k8 = k8b + 32 * u;
+          if (k8 < k8_end) {
+            const uint4 x8 = xr[k8];
+            const uint32_t wv[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+            const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
+            float part = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              part = fmaf(__uint_as_float(xv[q] << 16), __uint_as_float(wv[q] << 16), part);
+              part = fmaf(__uint_as_float(xv[q] & 0xffff0000u),
+                          __uint_as_float(wv[q] & 0xffff0000u), part);
+            }
+            acc += part;
+          }
+        }
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
