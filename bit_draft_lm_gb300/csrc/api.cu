@@ -108,6 +108,12 @@ int check_workspace(void* ws, size_t ws_bytes, int64_t M, const char* who) {
 
 }  // namespace
 
+namespace dh {
+// Records `msg` as the calling thread's dh_last_error() message and returns `code` (for entry
+// points defined in other files of the library).
+int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace dh
+
 extern "C" {
 
 int dh_quantize_pack_int2(const void* W, int64_t N, int64_t K, int G, uint8_t* packed, void* S,

@@ -42,5 +42,7 @@ cudaError_t launch_quantize_pack(int bits, const void* W, int64_t N, int64_t K, 
 // cudaErrorInvalidValue: the shape does not fit the kernel's shared-memory plan.
 cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s);
 cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s);
+// Sets the calling thread's dh_last_error() message; returns `code`.
+int record_error(int code, const char* msg);
 
 }  // namespace dh

@@ -43,6 +43,8 @@ SIGNATURES = {
                                    _SZ, _P], _I),
     "dh_draft_head_rerank_argmax": ([_P, _I64, _I64, _P, _I64, _P, _P, _I64, _I, _P, _P, _P, _P,
                                      _P, _SZ, _P], _I),
+    "dh_draft_head_rerank_argmax_noalloc": ([_P, _I64, _I64, _P, _I64, _P, _P, _I64, _I, _P,
+                                             _P, _P, _P, _P], _I),
     "dh_workspace_status": ([_P, _SZ, _P, _P], _I),
     "dh_last_error": ([], ctypes.c_char_p),
 }
@@ -210,6 +212,38 @@ def dh_draft_head_rerank_argmax(x: torch.Tensor, W: torch.Tensor, cand_val: torc
         _dev(argmax_id, "argmax_id", torch.int32, (M,)),
         _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    return rr_id, rr_logit, argmax_id
+
+
+def dh_draft_head_rerank_argmax_noalloc(x: torch.Tensor, W: torch.Tensor,
+                                        cand_val: torch.Tensor, cand_id: torch.Tensor,
+                                        rerank: int = 16, rr_id=None, rr_logit=None,
+                                        argmax_id=None, y_coarse=None, stream=None):
+    """dh_draft_head_rerank_argmax without a workspace: the library's fixed device scratch is
+    used instead (for callers that cannot allocate). Outputs are allocated here only when not
+    given. -> (rr_id i32 [M, R], rr_logit f32 [M, R], argmax_id i32 [M])."""
+    x = _bf16(x, "x")
+    W = _bf16(W, "W")
+    M, K = x.shape
+    N = W.shape[0]
+    ncand = cand_val.shape[1]
+    dev = x.device
+    if rr_id is None:
+        rr_id = torch.empty(M, rerank, dtype=torch.int32, device=dev)
+    if rr_logit is None:
+        rr_logit = torch.empty(M, rerank, dtype=torch.float32, device=dev)
+    if argmax_id is None:
+        argmax_id = torch.empty(M, dtype=torch.int32, device=dev)
+    if y_coarse is not None:
+        y_coarse = _bf16(y_coarse, "y_coarse")
+    _check(lib().dh_draft_head_rerank_argmax_noalloc(
+        _dev(x, "x", torch.bfloat16), M, K, _dev(W, "W", torch.bfloat16, (N, K)), N,
+        _dev(cand_val, "cand_val", torch.float32, (M, ncand)),
+        _dev(cand_id, "cand_id", torch.int32, (M, ncand)), ncand, rerank,
+        _dev(rr_id, "rr_id", torch.int32, (M, rerank)),
+        _dev(rr_logit, "rr_logit", torch.float32, (M, rerank)),
+        _dev(argmax_id, "argmax_id", torch.int32, (M,)),
+        _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)), _stream(stream)))
     return rr_id, rr_logit, argmax_id
 
 

@@ -128,6 +128,35 @@ int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void*
                                 void* y_coarse, void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
+ * Rerank + argmax without a caller workspace. The page has no counterpart to this entry point:
+ * it is for callers that cannot allocate device memory -- a plug-in handed only its input and
+ * output buffers, code running inside another framework's memory pool or allocator, or a
+ * caller whose allocator must not be entered at call time -- and so cannot provide the
+ * workspace that dh_draft_head_rerank_argmax takes.
+ *   Arguments, outputs and results are those of dh_draft_head_rerank_argmax (same kernels).
+ *   Workspace: a fixed array of DH_NOALLOC_SCRATCH_BYTES among the library's device globals;
+ *     every device that loads the library holds it until the process exits. Sizes whose
+ *     workspace (dh_workspace_bytes(M, N, K, 1, rerank)) exceeds it are rejected with
+ *     DH_ERR_SHAPE and a message; use dh_draft_head_rerank_argmax for those.
+ *   Set-up: the first call on a device, with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ *     capture on that device.
+ *   Each call clears the part of the array it uses (cudaMemsetAsync on s) and then launches;
+ *     nothing is allocated or freed.
+ *   All calls on a device share the one array and it keeps the last call's contents: calls
+ *     that overlap on the GPU (different streams without ordering between them) race on it and
+ *     give wrong results. Order them on one stream.
+ *   The device status word lives in the shared array and is not reported: an id >= N still
+ *     scores -inf, but DH_DEV_BAD_ID cannot be read back.
+ */
+#define DH_NOALLOC_SCRATCH_BYTES (1u << 20) /* 1 MiB per device */
+int dh_draft_head_rerank_argmax_noalloc(const void* x, int64_t M, int64_t K, const void* W,
+                                        int64_t N, const float* cand_val, const int32_t* cand_id,
+                                        int64_t ncand, int rerank, int32_t* rr_id,
+                                        float* rr_logit, int32_t* argmax_id, void* y_coarse,
+                                        dh_stream_t s);
+
+/*
  * Synchronises `s`, copies the workspace status word to *device_status and returns DH_OK if
  * it is zero, DH_ERR_DEVICE otherwise (DH_ERR_CUDA if the copy fails). The word is sticky:
  * zero the workspace to clear it.
