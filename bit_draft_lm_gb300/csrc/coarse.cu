@@ -26,10 +26,13 @@ static int plan_coarse(CoarseArgs& a, int max_smem, int nsw_max) {
   off += (kSBlocks + kMaxRedBufs) * 8 + (3 * kMaxRedBufs + kSBlocks + 2) * 4 + 16;
   a.off_xs = off = (off + 15) / 16 * 16;
   off += a.NW * 8 * 4 * 4;  // strip group sums: [NW][8 rows][<= 4 groups] fp32
+  off += mt_max * a.KG * 4;  // group sums of the row: [mt][K/G] fp32
+  a.off_zb = off = (off + 15) / 16 * 16;
+  off += (a.KG / 8) * 3 * mt_max * 4 * 8;  // zero-point MMA B fragments: [K/G/8][3][mt][4] uint2
   a.off_sz = off = (off + 127) / 128 * 128;
   off += kSBlocks * 2 * kBlockRows * a.KG * 2;
   a.off_red = off = (off + 15) / 16 * 16;
-  const int red_buf = a.NW * kBlockRows * a.red_pitch * 4;
+  const int red_buf = (a.NW + 1) * kBlockRows * a.red_pitch * 4;  // NW warps + zero-point slot
   const int wstage = kTileRows * SB;
   static const int kPlans[][2] = {{8, 4}, {8, 2}, {4, 4}, {4, 2}, {2, 2}};
   for (const auto& pl : kPlans) {
@@ -66,7 +69,6 @@ cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, 
   const int nsw = cc.bits == 2 ? plan_coarse<2>(a, max_smem, 8) : plan_coarse<4>(a, max_smem, 4);
   if (nsw < 2) return cudaErrorInvalidValue;
   if (a.NW < 1 || a.NW > kCoarseMaxWarps || a.KG % 8) return cudaErrorInvalidValue;
-  a.sh8_mul = 1u << 24;  // t >> 8
   a.u16_mul = 1u << 16;
   const int grid = a.nblk < num_sms ? a.nblk : num_sms;
   for (int m0 = 0; m0 < a.M; m0 += 8) {

@@ -12,8 +12,9 @@
 //        shared-memory stages with 16-byte cp.async copies, NSW-1 tiles ahead: no warp waits for
 //        another warp's weights.
 //  * S and ZS of a block (64 contiguous rows each) arrive by two bulk (TMA) copies into a ring of
-//    block stages. The last warp to finish block b (an arrival counter) knows that every warp is
-//    done with b's stage and partials; it refills the stage with the S and ZS of the block that
+//    block stages. The last arrival at the end of block b (an arrival counter: every warp, plus
+//    the zero-point pass) knows that every warp is done with b's stage and partials; it refills
+//    the stage with the S and ZS of the block that
 //    comes kSBlocks later and publishes b's epilogue as one job per hidden row. Warps claim jobs
 //    at block boundaries and while they wait (so the fastest warps do them, in parallel): a job
 //    sums the NW partials of its rows in a fixed order (deterministic), selects the top-KCAND
@@ -32,11 +33,19 @@
 //    two per hidden row (max |x * s| in [2^14, 2^15)): exact for every element above the f16
 //    normal threshold, i.e. for all but those below max |x| * 2^-29 (error < 2^-25 scaled).
 //  * The page's dequant is 1 + v/L (L = 4 for int2, 16 for int4) on the group's S and ZS: a group
-//    contributes S * (XS + sum x v / L) - ZS * XS = (S - ZS) * XS + S * sum x v / L. With the MMA
+//    contributes S * (XS + sum x v / L) - ZS * XS = S * sum x v / L + (S - ZS) * XS. With the MMA
 //    result D = s * 2^-24 * sum x v per (plane, group) of the strip, the warp accumulates
-//    acc = sum S * D - sum (ZS - S) * XS * s / kappa and the logit is y = (kappa / s) * acc, with
-//    kappa = 2^24 / L: powers of two, exact. Only one of the warps whose strips cover a group (its
-//    "owner") adds that group's zero-point term.
+//    acc = sum S * D and its partial of the row is (kappa / s) * acc, kappa = 2^24 / L (powers of
+//    two, exact). The zero-point part Z = sum_g (S - ZS) * XS of a 16-row tile is one more short
+//    MMA chain: A = the tile's S and ZS rows as they are (bf16, K/G + K/G columns), B = XS and
+//    -XS split exactly into three bf16 parts (hi, mid, lo), fp32 accumulation. The first warp to
+//    finish a block runs it for the block's four tiles and writes it to an extra partial slot,
+//    so the per-tile loop has no zero-point work and no per-tile branch.
+//  * One hidden row (M = 1): the MMA's 8 columns would be 7/8 idle, so each scale group of the
+//    strip gets its own column instead. Lane column g of the B operand holds x for the planes of
+//    scale group g and zeros elsewhere, so one accumulator collects every plane of the tile, each
+//    in its own column, and the per-group scale is applied once per tile per group (lanes
+//    c = 0, 1 hold columns 0..3), not once per plane per accumulator register.
 //  * The per-group scale is applied to the accumulator, never to the weight tile.
 // Hidden rows are processed eight at a time (one MMA column tile); M > 8 runs ceil(M/8) passes.
 #pragma once
@@ -70,13 +79,14 @@ struct CoarseArgs {
   int32_t* cand_id;
   uint16_t* y;  // bf16 [M, N] or nullptr
   uint32_t* status;
-  // 2^24 (t >> 8 as the high word of a product) and 2^16 (bf16 bits -> fp32): kernel parameters,
-  // so that these stay integer multiplies on the FMA pipe instead of shifts on the ALU pipe,
-  // which the dequant's ANDs keep busy.
-  uint32_t sh8_mul, u16_mul;
+  // 2^16 (bf16 bits -> fp32): a kernel parameter, so that the conversion stays an integer
+  // multiply on the FMA pipe instead of a shift on the ALU pipe, which the dequant's ANDs keep
+  // busy. (The t >> 8 of the odd bytes is a shift: an integer multiply-high runs at a quarter of
+  // the ALU rate and stalls the tensor pipe's MMAs.)
+  uint32_t u16_mul;
   // shared-memory plan
   int nb, red_pitch;
-  int off_bars, off_xs, off_sz, off_red, off_ring;
+  int off_bars, off_xs, off_zb, off_sz, off_red, off_ring;
 };
 
 // 16-byte copy global -> shared (shared-space address); valid = false copies zeros.
@@ -111,28 +121,27 @@ __host__ __device__ constexpr int plane_shift(int p) {
 // G: the quantisation group (64 or 128). KSPEC: the hidden size K when it is known at compile
 // time (the vocabulary-scale head), 0 for a runtime K: with K fixed, every shared-memory offset
 // and stride below is an immediate. NSW: stages of each warp's private weight ring. MT1: a single
-// hidden row in this pass.
+// hidden row in this pass (scale groups in the MMA's columns).
 template <int BITS, int G, int KSPEC, int NSW, bool MT1>
 __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const CoarseArgs a) {
   // SPLIT: the strip spans two quantisation groups per plane (int4 with G = 64), so the
   // accumulator is folded once per 64-byte sub-chunk instead of once per strip.
-  // OWNHALF: a group spans the strips of two warps (int2 with G = 128); the warp whose parity is
-  // that of plane p owns plane p's zero-point term.
   constexpr bool SPLIT = BITS == 4 && G == 64;
-  constexpr bool OWNHALF = BITS == 2 && G == 128;
   constexpr int P = 8 / BITS;             // codes per byte (planes)
   constexpr int SB = 256 / P;             // strip bytes per row: 256 k-values
   constexpr int U = SB / 64;              // 64-byte sub-chunks per strip
   constexpr int FS = SPLIT ? U : 1;       // fold segments per strip
-  constexpr int NQ = FS * P;              // scale groups per strip
+  constexpr int NQ = FS * P;              // scale groups per strip (<= 4)
   constexpr int WSTAGE = kTileRows * SB;  // packed bytes of one warp's strip of a tile
   constexpr int CH = WSTAGE / 16 / 32;    // 16-byte weight copies per lane per tile
   constexpr int kLogL = BITS == 2 ? 2 : 4;  // log2 of the page's divisor L
+  constexpr int KGS = KSPEC ? KSPEC / G : 0;  // K/G when K is compiled in
   static_assert((NSW & (NSW - 1)) == 0, "ring depth must be a power of two");
+  static_assert(NQ <= 4, "scale groups of a strip must fit columns 0..3");
   extern __shared__ __align__(128) unsigned char sm[];
 
   const int K = KSPEC ? KSPEC : a.K;  // hidden size
-  const int NW = K / 256, KG = K / G, RB = K * BITS / 8;
+  const int NW = K / 256, KG = KSPEC ? KGS : K / G, RB = K * BITS / 8;
   const int mt = MT1 ? 1 : a.mt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -146,15 +155,16 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   int* jobs_ready = job_pub + kMaxRedBufs;   // jobs [0, jobs_ready) may run
   int* jobs_claimed = jobs_ready + 1;        // jobs [0, jobs_claimed) taken by some warp
   volatile int* abort_flag = jobs_claimed + 1;
-  float* xs_half = reinterpret_cast<float*>(sm + a.off_xs);  // [NW][8][NQ] strip group sums
+  float* xs_part = reinterpret_cast<float*>(sm + a.off_xs);  // [NW][8][NQ] strip group sums
+  float* xs_full = xs_part + NW * 8 * NQ;                    // [mt][KG] group sums XS
+  uint2* zb = reinterpret_cast<uint2*>(sm + a.off_zb);  // [KG/8][3][mt][4] B fragments of Z
   unsigned char* sz = sm + a.off_sz;                      // [kSBlocks][S|ZS][64][KG] bf16
-  float* red = reinterpret_cast<float*>(sm + a.off_red);  // [nb][NW][64][rp]
+  float* red = reinterpret_cast<float*>(sm + a.off_red);  // [nb][NW + 1][64][rp]
   const int sz_half = kBlockRows * KG * 2;                // bytes of a stage's S (or ZS) rows
   const int red_wstride = kBlockRows * rp;
 
   const int my_blocks = (a.nblk - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                         static_cast<int>(gridDim.x);
-  const int my_tiles = my_blocks * kTilesPerBlock;
   auto block_row0 = [&](int lb) {
     return (static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x)) * kBlockRows;
   };
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     for (int lb = 0; lb < kSBlocks && lb < my_blocks; ++lb) issue_sz(lb);
   }
 
-  // ---- weight streaming of tile tau into ring stage tau % NSW, by warp `warp` alone:
+  // ---- weight streaming of tile tau = 4 lb + t into ring stage tau % NSW, by warp `warp` alone:
   // chunk e = lane + 32 j is row e / (SB/16), 16-byte column e % (SB/16) of the warp's strip;
   // int4 rows are XOR-swizzled by (row & 1) so the two rows one quarter-warp reads use disjoint
   // banks; rows past N are zero-filled.
@@ -200,29 +210,28 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   const int pcol0 = BITS == 4 ? (col0 ^ ((r0l & 1) << 2)) : col0;
   const uint32_t dst_lane =
       smem_addr(sm + a.off_ring + warp * (NSW * WSTAGE)) + r0l * SB + 16 * pcol0;
-  const int64_t src_lane = static_cast<int64_t>(r0l) * RB + strip_byte + 16 * col0;
-  const int64_t src_jstep = static_cast<int64_t>(RPJ) * RB;
-  auto load_tile = [&](int tau) {
-    if (tau < my_tiles) {
-      const int row0 = block_row0(tau >> 2) + (tau & 3) * kTileRows;
-      const uint8_t* src = a.packed + static_cast<int64_t>(row0) * RB + src_lane;
-      const uint32_t dst = dst_lane + (tau & (NSW - 1)) * WSTAGE;
-      if (row0 + kTileRows <= a.N) {
+  const int src_lane = strip_byte + 16 * col0;
+  // tile tk of local block lbk into ring stage (4 lbk + tk) % NSW. Past this CTA's blocks the
+  // copies read nothing (zero-fill); rows past N re-read row N - 1 (their values are ignored).
+  auto load_tile = [&](int lbk, int tk) {
+    const bool live = lbk < my_blocks;
+    const int row = block_row0(lbk) + tk * kTileRows + r0l;
+    const uint32_t dst = dst_lane + ((4 * lbk + tk) & (NSW - 1)) * WSTAGE;
 #pragma unroll
-        for (int j = 0; j < CH; ++j) cp_async16(dst + j * RPJ * SB, src + j * src_jstep, true);
-      } else {
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const bool ok = row0 + r0l + j * RPJ < a.N;
-          cp_async16(dst + j * RPJ * SB, ok ? src + j * src_jstep : a.packed, ok);
-        }
-      }
+    for (int j = 0; j < CH; ++j) {
+      const int rj = min(row + j * RPJ, a.N - 1);
+      cp_async16(dst + j * RPJ * SB, live ? a.packed + static_cast<int64_t>(rj) * RB + src_lane
+                                          : a.packed,
+                 live);
     }
     cp_async_commit();  // one group per tile slot, possibly empty, keeps the counting uniform
   };
-  // ---- this warp's view of x (hidden row g, lanes g < mt), loaded before the weight prefetch so
-  // that it does not queue behind it: the strip's values for the MMA's B operand.
-  const uint16_t* xg = a.x + static_cast<int64_t>(a.m0 + (g < mt ? g : 0)) * K;  // hidden row g
+  // ---- this warp's view of x, loaded before the weight prefetch so that it does not queue
+  // behind it: the strip's values for the MMA's B operand. Lanes of column g hold hidden row g
+  // (zeros for g >= mt); with one hidden row every lane holds it.
+  const int xrow = MT1 ? 0 : (g < mt ? g : 0);
+  const bool xval = MT1 || g < mt;
+  const uint16_t* xg = a.x + static_cast<int64_t>(a.m0 + xrow) * K;
   uint2 xv[U][4][P];
 #pragma unroll
   for (int u = 0; u < U; ++u)
@@ -230,12 +239,12 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int p = 0; p < P; ++p)
-        xv[u][i][p] = g < mt ? *reinterpret_cast<const uint2*>(
-                                   xg + p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i)
-                             : make_uint2(0u, 0u);
+        xv[u][i][p] = xval ? *reinterpret_cast<const uint2*>(
+                                 xg + p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i)
+                           : make_uint2(0u, 0u);
 
 #pragma unroll
-  for (int t = 0; t < NSW - 1; ++t) load_tile(t);
+  for (int t = 0; t < NSW - 1; ++t) load_tile(t / kTilesPerBlock, t % kTilesPerBlock);
 
   // S column of scale group q = (fold segment f, plane p) of this strip: p*(RB/G) + (strip+64f)/G
   auto s_col = [&](int q) {
@@ -243,13 +252,14 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   };
   auto pow2 = [](int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); };
 
-  // B operand: x of hidden row g for strip bytes 64u + 16c + 4i + {0, 2} (register 0) and
-  // {1, 3} (register 1), plane p, as f16 x * s / 2^plane_shift(p). Each warp scales by its own
-  // power of two s = 2^(15 - E), max |x| = f * 2^E (f in [0.5, 1)) over its strip of the row,
-  // and converts its partials to logit units before storing them. Also the sums of x over the
-  // strip's part of each scale group q (the zero-point term).
+  // B operand: x of the lane's hidden row for strip bytes 64u + 16c + 4i + {0, 2} (register 0)
+  // and {1, 3} (register 1), plane p, as f16 x * s / 2^plane_shift(p). Each warp scales by its
+  // own power of two s = 2^(15 - E), max |x| = f * 2^E (f in [0.5, 1)) over its strip of the
+  // row, and converts its partials to logit units before storing them. With one hidden row,
+  // column g keeps only the values of scale group q = g (zeros elsewhere). Also the sums of x
+  // over the strip's part of each scale group q.
   uint32_t bfr[U][4][P][2];
-  int ew;  // E of this warp's strip of hidden row g
+  int ew;  // E of this warp's strip of the lane's hidden row
   float xsg[NQ];
   {
     uint32_t mx = 0;  // max |x| as bf16 magnitude bits (monotone in the value)
@@ -289,38 +299,115 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             hs[e] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(h[e]) * sx));
-          bfr[u][i][p][0] = hs[0] | (hs[2] << 16);  // (x[k0], x[k0+2]): even bytes of the word
-          bfr[u][i][p][1] = hs[1] | (hs[3] << 16);  // (x[k0+1], x[k0+3]): odd bytes
+          const bool keep = !MT1 || ((SPLIT ? u * P : 0) + p) == g;
+          bfr[u][i][p][0] = keep ? hs[0] | (hs[2] << 16) : 0u;  // (x[k0], x[k0+2]): even bytes
+          bfr[u][i][p][1] = keep ? hs[1] | (hs[3] << 16) : 0u;  // (x[k0+1], x[k0+3]): odd bytes
         }
   }
-  // A group of 128 int2 k-values spans the strips of warps 2j, 2j+1: the halves meet in shared
-  // memory (lower warp's half first, a fixed order).
-  if (OWNHALF && c == 0) {
+  // Group sums XS[m][col] of the whole row (for the zero-point MMA): each warp publishes its
+  // strip's part, then the parts of each group are added in warp order (deterministic).
+  if (c == 0 && g < mt) {
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) xs_half[(warp * 8 + g) * NQ + q] = xsg[q];
+    for (int q = 0; q < NQ; ++q) xs_part[(warp * 8 + g) * NQ + q] = xsg[q];
   }
   __syncthreads();  // barriers initialised, strip sums published
-  if (OWNHALF) {
-    const int w0 = warp & ~1;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q)
-      xsg[q] = xs_half[(w0 * 8 + g) * NQ + q] + xs_half[((w0 + 1) * 8 + g) * NQ + q];
+  {
+    const int RBG = RB / G;  // groups per plane
+    for (int e = threadIdx.x; e < mt * KG; e += blockDim.x) {
+      const int m = e / KG, col = e - m * KG;
+      const int p = col / RBG, r0 = (col - p * RBG) * G;  // plane, first byte of the group
+      float sum = 0.0f;
+      for (int w = r0 / SB; w <= (r0 + G - 1) / SB; ++w) {
+        const int f = SPLIT ? (r0 - w * SB) / 64 : 0;
+        sum += xs_part[(w * 8 + m) * NQ + f * P + p];
+      }
+      xs_full[m * KG + col] = sum;
+    }
   }
+  __syncthreads();
+  // B fragments of the zero-point MMA: k' < KG is +XS[k'] (against S), KG <= k' < 2KG is
+  // -XS[k' - KG] (against ZS); each value split exactly into bf16 hi + mid + lo.
+  for (int e = threadIdx.x; e < (KG / 8) * 3 * mt * 4; e += blockDim.x) {
+    const int cc = e & 3, m = (e >> 2) % mt, kp = (e >> 2) / mt;  // kp = kk * 3 + part
+    const int kk = kp / 3, part = kp - kk * 3;
+    uint32_t r[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t hv[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int kq = 16 * kk + 8 * h + 2 * cc + j;
+        float v = kq < KG ? xs_full[m * KG + kq] : -xs_full[m * KG + kq - KG];
+        float pv = 0.0f;
+        for (int q = 0; q <= part; ++q) {
+          pv = __bfloat162float(__float2bfloat16_rn(v));
+          v -= pv;  // exact: v and pv share the leading bits
+        }
+        hv[j] = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+      }
+      r[h] = hv[0] | (hv[1] << 16);
+    }
+    zb[e] = make_uint2(r[0], r[1]);
+  }
+  __syncthreads();
 
-
-  // byte offset of this lane's S entry of group (f, p) in a stage: so0 + p * pstride + 2 f
+  // byte offset of this lane's S entry of scale group q in a stage: so_g + 2 * s_col(q)
   // (row g of tile t adds t * 16 rows; row g + 8 adds row8)
-  const int so0 = g * KG * 2 + 2 * s_col(0);
-  const int pstride = 2 * (RB / G);
+  const int so_g = g * KG * 2;
   const int row8 = 8 * KG * 2;
   const unsigned char* ring = sm + a.off_ring + warp * (NSW * WSTAGE);
-  float* rw_base = red + warp * red_wstride + g * rp + 2 * c;
+  float* rw_base = red + warp * red_wstride + g * rp + (MT1 ? 0 : 2 * c);
 
-  // ---- epilogue job: top-KCAND of hidden row m of local block lb, partials in buf
+  // ---- zero-point part of a block, in logit units, into partial slot `zs` ([64][rp]): per
+  // 16-row tile, sum over groups of (S - ZS) * XS as A = [S | ZS] (bf16, as stored) times
+  // B = [XS ; -XS] in three bf16 parts; D layout (rows g, g + 8 x hidden rows 2c, 2c + 1).
+  auto zero_point_block = [&](const unsigned char* stage, float* zs) {
+    const uint2* zl = zb + (g < mt ? g : 0) * 4 + c;
+    const bool zlive = g < mt;
+#pragma unroll 1
+    for (int t = 0; t < kTilesPerBlock; ++t) {
+      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const unsigned char* srow = stage + (t * kTileRows + g) * KG * 2 + 4 * c;
+      for (int kk = 0; kk < KG / 8; ++kk) {
+        uint32_t av[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int o8 = 16 * kk + 8 * h;  // first column of the octet (all S or all ZS)
+          const unsigned char* src = o8 < KG ? srow + 2 * o8 : srow + sz_half + 2 * (o8 - KG);
+          av[2 * h] = *reinterpret_cast<const uint32_t*>(src);
+          av[2 * h + 1] = *reinterpret_cast<const uint32_t*>(src + row8);
+        }
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const uint2 b = zlive ? zl[(kk * 3 + part) * mt * 4] : make_uint2(0u, 0u);
+          mma_bf16_16816_acc(z, av[0], av[1], av[2], av[3], b.x, b.y);
+        }
+      }
+      float* zw = zs + (t * kTileRows + g) * rp + (MT1 ? 0 : 2 * c);
+      if (MT1) {
+        if (c == 0) {
+          zw[0] = z[0];
+          zw[8] = z[2];
+        }
+      } else {
+        if (2 * c < mt) {
+          zw[0] = z[0];
+          zw[8 * rp] = z[2];
+        }
+        if (2 * c + 1 < mt) {
+          zw[1] = z[1];
+          zw[8 * rp + 1] = z[3];
+        }
+      }
+    }
+  };
+
+  // ---- epilogue job: top-KCAND of hidden row m of local block lb, partials in buf (the NW
+  // warps' and the zero-point slot)
   auto epilogue = [&](int lb, int buf, int m) {
     const int b = static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x);
     const int n0 = b * kBlockRows + lane;
-    const float* rbuf = red + buf * NW * red_wstride;
+    const float* rbuf = red + buf * (NW + 1) * red_wstride;
     {
       float v[2];
 #pragma unroll
@@ -329,13 +416,13 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
         const float* rb = rbuf + (lane + 32 * h) * rp + m;
         float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
         int w = 0;
-        for (; w + 4 <= NW; w += 4) {
+        for (; w + 4 <= NW + 1; w += 4) {
           s0 += rb[w * red_wstride];
           s1 += rb[(w + 1) * red_wstride];
           s2 += rb[(w + 2) * red_wstride];
           s3 += rb[(w + 3) * red_wstride];
         }
-        for (; w < NW; ++w) s0 += rb[w * red_wstride];
+        for (; w < NW + 1; ++w) s0 += rb[w * red_wstride];
         v[h] = (s0 + s1) + (s2 + s3);
       }
       if (a.y) {
@@ -433,119 +520,167 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     }
   };
 
-  auto run = [&](auto par_tag) {
-    constexpr int PAR = decltype(par_tag)::value;
-    // For the lane's accumulator columns (hidden rows 2c, 2c + 1): the zero-point weights
-    // XS * s / kappa = XS * 2^(15 - E) * 2^(logL - 24) of the owned groups, and the factor
-    // kappa / s that turns the partials into logits.
-    float xsv[NQ][2], ysc[2];
+  // factor kappa / s that turns this lane's partials into logits: hidden rows 2c, 2c + 1 (MT1:
+  // the one hidden row, in ysc[0])
+  float ysc[2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int hr = 2 * c + j, src = (hr < 8 ? hr : 0) * 4;
-      const int e = __shfl_sync(0xffffffffu, ew, src);
-      ysc[j] = hr < mt ? pow2(e + 9 - kLogL) : 0.0f;
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        const float xs = __shfl_sync(0xffffffffu, xsg[q], src);
-        xsv[q][j] = (!OWNHALF || ((q % P) & 1) == PAR) && hr < mt ? xs * pow2(kLogL - 9 - e) : 0.0f;
-      }
+  for (int j = 0; j < 2; ++j) {
+    const int hr = MT1 ? 0 : 2 * c + j, src = (hr < 8 ? hr : 0) * 4;
+    const int e = __shfl_sync(0xffffffffu, ew, src);
+    ysc[j] = hr < mt ? pow2(e + 9 - kLogL) : 0.0f;
+  }
+  // MT1: the two scale groups (columns 2c, 2c + 1) this lane folds; lanes past NQ/2 hold zero
+  // columns and fold a valid group's scale into them (no effect).
+  const int qa = MT1 ? (2 * c < NQ ? 2 * c : 0) : 0;
+  const int soa = so_g + 2 * s_col(qa), sob = so_g + 2 * s_col(qa + 1 < NQ ? qa + 1 : qa);
+  // The last of the block's NW + 1 arrivals (every warp, plus the zero-point pass) refills the
+  // block's S/ZS stage and publishes its epilogue jobs. Lane 0.
+  auto finish_block = [&](int lb, int buf) {
+    blk_cnt[buf] = 0;
+    __threadfence_block();
+    if (lb + kSBlocks < my_blocks) {
+      fence_proxy_async_smem();  // stage reads happen before the copy's writes
+      issue_sz(lb + kSBlocks);
     }
-    for (int tau = 0; tau < my_tiles; ++tau) {
-      load_tile(tau + NSW - 1);  // into the stage the previous tile freed
-      cp_async_wait<NSW - 1>();  // tile tau has landed (for this lane's copies)
-      __syncwarp();              // ... and for every lane's
-      const int t = tau & 3, lb = tau >> 2, buf = lb & (nb - 1);
-      const int sst = lb % kSBlocks;
-      if (t == 0) {
-        bool ok = wait_taking_jobs(&full_sb[sst], static_cast<uint32_t>(lb / kSBlocks) & 1u);
-        if (ok && lb >= nb)
-          ok = wait_taking_jobs(&red_empty[buf], static_cast<uint32_t>(lb / nb - 1) & 1u);
-        if (!ok) break;
-        try_job(false);  // an epilogue another warp published, if one is ready
-      }
+    job_pub[buf] = warp;
+    __threadfence_block();
+    atomicMax(jobs_ready, (lb + 1) * mt);
+  };
 
-      const unsigned char* cs = ring + (tau & (NSW - 1)) * WSTAGE;  // this warp's stage
-      const unsigned char* szs = sz + sst * 2 * sz_half + t * (kTileRows * KG * 2) + so0;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      float d[P][4];
+  for (int lb = 0; lb < my_blocks; ++lb) {
+    const int buf = lb & (nb - 1), sst = lb % kSBlocks;
+    {
+      bool ok = wait_taking_jobs(&full_sb[sst], static_cast<uint32_t>(lb / kSBlocks) & 1u);
+      if (ok && lb >= nb)
+        ok = wait_taking_jobs(&red_empty[buf], static_cast<uint32_t>(lb / nb - 1) & 1u);
+      if (!ok) break;
+      try_job(false);  // an epilogue another warp published, if one is ready
+    }
+    const unsigned char* stage = sz + sst * 2 * sz_half;
+    float* rwb = rw_base + buf * (NW + 1) * red_wstride;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int pc = BITS == 4 ? ((4 * u + c) ^ ((g & 1) << 2)) : c;  // swizzled column
-        const uint4 wa = *reinterpret_cast<const uint4*>(cs + g * SB + 16 * pc);
-        const uint4 wb = *reinterpret_cast<const uint4*>(cs + (g + 8) * SB + 16 * pc);
-        const uint32_t ta[4] = {wa.x, wa.y, wa.z, wa.w}, tb[4] = {wb.x, wb.y, wb.z, wb.w};
-        uint32_t tao[4], tbo[4];  // odd bytes moved down: t >> 8 (the multiply's high word)
+    for (int t = 0; t < kTilesPerBlock; ++t) {
+      constexpr int kAhead = NSW - 1;
+      load_tile(lb + (t + kAhead) / kTilesPerBlock, (t + kAhead) % kTilesPerBlock);
+      cp_async_wait<NSW - 1>();  // tile (lb, t) has landed (for this lane's copies)
+      __syncwarp();              // ... and for every lane's
+      const unsigned char* cs = ring + ((kTilesPerBlock * lb + t) & (NSW - 1)) * WSTAGE;
+      const unsigned char* szs = stage + t * (kTileRows * KG * 2);
+      float acc[4];
+      if (MT1) {
+        // every plane of the tile into one accumulator (scale group q in column q), two chains
+        float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tao[i] = __umulhi(ta[i], a.sh8_mul);
-          tbo[i] = __umulhi(tb[i], a.sh8_mul);
-        }
-        const int f = SPLIT ? u : 0;
-        const bool seg_first = SPLIT || u == 0, seg_last = SPLIT || u == U - 1;
-        // plane by plane: the plane's accumulator is folded as soon as its segment is complete
+        for (int u = 0; u < U; ++u) {
+          const int pc = BITS == 4 ? ((4 * u + c) ^ ((g & 1) << 2)) : c;  // swizzled column
+          const uint4 wa = *reinterpret_cast<const uint4*>(cs + g * SB + 16 * pc);
+          const uint4 wb = *reinterpret_cast<const uint4*>(cs + (g + 8) * SB + 16 * pc);
+          const uint32_t ta[4] = {wa.x, wa.y, wa.z, wa.w}, tb[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-          if (seg_first) {
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t tao = ta[i] >> 8, tbo = tb[i] >> 8;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[p][e] = 0.0f;
+            for (int p = 0; p < P; ++p)
+              mma_f16_16816_acc((i & 1) ? d1 : d0, dq16<BITS>(ta[i], p), dq16<BITS>(tb[i], p),
+                                dq16<BITS>(tao, p), dq16<BITS>(tbo, p), bfr[u][i][p][0],
+                                bfr[u][i][p][1]);
           }
+        }
+        // d: (row g, group 2c), (row g, group 2c+1), (row g+8, group 2c), (row g+8, group 2c+1)
+        const float sa = __uint_as_float(lds_u16(szs + soa) * a.u16_mul);
+        const float sb = __uint_as_float(lds_u16(szs + sob) * a.u16_mul);
+        const float sa8 = __uint_as_float(lds_u16(szs + soa + row8) * a.u16_mul);
+        const float sb8 = __uint_as_float(lds_u16(szs + sob + row8) * a.u16_mul);
+        float r0 = fmaf(sb, d0[1] + d1[1], sa * (d0[0] + d1[0]));
+        float r8 = fmaf(sb8, d0[3] + d1[3], sa8 * (d0[2] + d1[2]));
+        if (NQ > 2) {  // groups 2, 3 sit in lane c = 1
+          r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+          r8 += __shfl_xor_sync(0xffffffffu, r8, 1);
+        }
+        acc[0] = r0;
+        acc[2] = r8;
+        acc[1] = acc[3] = 0.0f;
+      } else {
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+        float d[P][4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mma_f16_16816_acc(d[p], dq16<BITS>(ta[i], p), dq16<BITS>(tb[i], p),
-                              dq16<BITS>(tao[i], p), dq16<BITS>(tbo[i], p), bfr[u][i][p][0],
-                              bfr[u][i][p][1]);
-          if (seg_last) {
-            // fold: acc += S * D; the owner subtracts (ZS - S) * XS * s / kappa
-            const int q = f * P + p;
-            const unsigned char* sq = szs + p * pstride + 2 * f;
-            const float sg = __uint_as_float(lds_u16(sq) * a.u16_mul);
-            const float sg8 = __uint_as_float(lds_u16(sq + row8) * a.u16_mul);
-            acc[0] = fmaf(sg, d[p][0], acc[0]);
-            acc[1] = fmaf(sg, d[p][1], acc[1]);
-            acc[2] = fmaf(sg8, d[p][2], acc[2]);
-            acc[3] = fmaf(sg8, d[p][3], acc[3]);
-            if (!OWNHALF || (p & 1) == PAR) {
-              const float zc = __uint_as_float(lds_u16(sq + sz_half) * a.u16_mul) - sg;
-              const float zc8 = __uint_as_float(lds_u16(sq + sz_half + row8) * a.u16_mul) - sg8;
-              acc[0] = fmaf(-zc, xsv[q][0], acc[0]);
-              acc[1] = fmaf(-zc, xsv[q][1], acc[1]);
-              acc[2] = fmaf(-zc8, xsv[q][0], acc[2]);
-              acc[3] = fmaf(-zc8, xsv[q][1], acc[3]);
+        for (int u = 0; u < U; ++u) {
+          const int pc = BITS == 4 ? ((4 * u + c) ^ ((g & 1) << 2)) : c;  // swizzled column
+          const uint4 wa = *reinterpret_cast<const uint4*>(cs + g * SB + 16 * pc);
+          const uint4 wb = *reinterpret_cast<const uint4*>(cs + (g + 8) * SB + 16 * pc);
+          const uint32_t ta[4] = {wa.x, wa.y, wa.z, wa.w}, tb[4] = {wb.x, wb.y, wb.z, wb.w};
+          uint32_t tao[4], tbo[4];  // odd bytes moved down: t >> 8
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            tao[i] = ta[i] >> 8;
+            tbo[i] = tb[i] >> 8;
+          }
+          const int f = SPLIT ? u : 0;
+          const bool seg_first = SPLIT || u == 0, seg_last = SPLIT || u == U - 1;
+          // plane by plane: the plane's accumulator is folded as soon as its segment is complete
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            if (seg_first) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d[p][e] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma_f16_16816_acc(d[p], dq16<BITS>(ta[i], p), dq16<BITS>(tb[i], p),
+                                dq16<BITS>(tao[i], p), dq16<BITS>(tbo[i], p), bfr[u][i][p][0],
+                                bfr[u][i][p][1]);
+            if (seg_last) {
+              const unsigned char* sq = szs + so_g + 2 * s_col(f * P + p);
+              const float sg = __uint_as_float(lds_u16(sq) * a.u16_mul);
+              const float sg8 = __uint_as_float(lds_u16(sq + row8) * a.u16_mul);
+              acc[0] = fmaf(sg, d[p][0], acc[0]);
+              acc[1] = fmaf(sg, d[p][1], acc[1]);
+              acc[2] = fmaf(sg8, d[p][2], acc[2]);
+              acc[3] = fmaf(sg8, d[p][3], acc[3]);
             }
           }
         }
       }
-      // partials, D layout: acc[0..1] = row g, hidden rows 2c, 2c+1; acc[2..3] = row g + 8
-      float* rw = rw_base + (buf * NW * kBlockRows + t * kTileRows) * rp;
-      if (2 * c < mt) {
-        rw[0] = acc[0] * ysc[0];
-        rw[8 * rp] = acc[2] * ysc[0];
-      }
-      if (2 * c + 1 < mt) {
-        rw[1] = acc[1] * ysc[1];
-        rw[8 * rp + 1] = acc[3] * ysc[1];
-      }
-      if (t == kTilesPerBlock - 1) {
-        // end of block lb for this warp. The last warp to get here refills the block's S/ZS
-        // stage and publishes the block's epilogue jobs.
-        __syncwarp();  // every lane's partial stores and stage reads are done
-        if (lane == 0) {
-          __threadfence_block();
-          if (atomicAdd(&blk_cnt[buf], 1) == NW - 1) {
-            blk_cnt[buf] = 0;
-            __threadfence_block();
-            if (lb + kSBlocks < my_blocks) {
-              fence_proxy_async_smem();  // stage reads happen before the copy's writes
-              issue_sz(lb + kSBlocks);
-            }
-            job_pub[buf] = warp;
-            __threadfence_block();
-            atomicMax(jobs_ready, (lb + 1) * mt);
-          }
+      // partials in logit units, D layout: acc[0..1] = row g, hidden rows 2c, 2c+1; acc[2..3] =
+      // row g + 8 (MT1: acc[0], acc[2] in lane c = 0)
+      float* rw = rwb + t * kTileRows * rp;
+      if (MT1) {
+        if (c == 0) {
+          rw[0] = acc[0] * ysc[0];
+          rw[8] = acc[2] * ysc[0];
+        }
+      } else {
+        if (2 * c < mt) {
+          rw[0] = acc[0] * ysc[0];
+          rw[8 * rp] = acc[2] * ysc[0];
+        }
+        if (2 * c + 1 < mt) {
+          rw[1] = acc[1] * ysc[1];
+          rw[8 * rp + 1] = acc[3] * ysc[1];
         }
       }
     }
-    // drain: take epilogue jobs until every job of this CTA has been taken by some warp
+    // end of block lb for this warp: the first warp here also computes the block's zero-point
+    // slot (the S/ZS stage stays until every arrival, that pass's included, is in)
+    __syncwarp();  // every lane's partial stores and stage reads are done
+    int first = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      const int old = atomicAdd(&blk_cnt[buf], 1);
+      first = old == 0;
+      if (old == NW) finish_block(lb, buf);
+    }
+    if (__shfl_sync(0xffffffffu, first, 0)) {
+      zero_point_block(stage, red + buf * (NW + 1) * red_wstride + NW * red_wstride);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        if (atomicAdd(&blk_cnt[buf], 1) == NW) finish_block(lb, buf);
+      }
+    }
+  }
+  // drain: take epilogue jobs until every job of this CTA has been taken by some warp
+  {
     const uint64_t t0 = global_timer_ns();
     while (true) {
       int st = 0;
@@ -559,11 +694,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
         set_status(a.status, DH_DEV_WAIT_TIMEOUT);
       }
     }
-  };
-  if (OWNHALF && (warp & 1))
-    run(std::integral_constant<int, 1>{});
-  else
-    run(std::integral_constant<int, 0>{});
+  }
   cp_async_wait<0>();
   // After an abort, S/ZS copies may still be in flight: they must land before the CTA's shared
   // memory goes away. (Normally every issued stage has been waited for already.)

@@ -14,6 +14,7 @@
 //     slice sums added in a fixed order;
 //  4. argmax over the rescored values (ties to the lowest vocab id) and the optional scatter of
 //     bf16(logit) into the coarse logits.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,6 +24,8 @@
 #include "dh_launch.h"
 
 namespace dh {
+
+namespace cg = cooperative_groups;
 
 constexpr int kRerankThreads = 1024;
 constexpr int kRerankWarps = kRerankThreads / 32;
@@ -331,6 +334,286 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
 }
 
 
+
+// ---- Cluster path (R <= 32, ncand <= 16384): one cluster of kRC CTAs per hidden row. The CTAs
+// split the row's candidate slots, coordinate through distributed shared memory (no global
+// round trips between phases) and each computes R / kRC of the exact dots:
+//  1. every CTA loads its slots (keys and ids in registers) and its copy of x; its warp maxima
+//     go to CTA 0;
+//  2. CTA 0 takes T = the R-th largest of the kRC * 8 warp maxima (a lower bound of the R-th
+//     largest candidate, as in the single-CTA kernel) and sends it to every CTA;
+//  3. every CTA appends its candidates with key >= T to CTA 0's survivor list;
+//  4. CTA 0 selects the R first survivors in the selection order (or, if the list overflowed,
+//     runs the exact R-round selection over the whole row) and sends the ids to every CTA;
+//  5. CTA r computes the dots of slots r, r + kRC, ...; CTA 0 takes the argmax.
+constexpr int kRC = 8;
+constexpr int kRCThreads = 256;
+constexpr int kRCWarps = kRCThreads / 32;
+constexpr int kRCMaxLPT = 8;
+constexpr int kRCSurvCap = 256;
+constexpr int kRCMaxR = 32;
+constexpr int kRCMaxCand = kRC * kRCThreads * kRCMaxLPT;  // 16384
+
+struct RCShared {
+  uint32_t allmax[kRC * kRCWarps];  // CTA 0: warp maxima of the cluster
+  uint32_t T;                       // threshold (every CTA)
+  int surv_n;                       // CTA 0: survivors appended
+  int base;                         // this CTA's first survivor position
+  int wcnt[kRCWarps];
+  Sel surv[kRCSurvCap];          // CTA 0: survivors
+  Sel wbest[kRCWarps + 1];       // CTA 0 slow path
+  int32_t rr[kRCMaxR];           // selected ids (every CTA)
+  float part[4][kRCWarps];       // dot partials per warp, up to 4 slots per CTA
+  float logit[kRCMaxR];          // CTA 0: reranked logits
+  uint32_t retired[kRCMaxCand / 32];  // CTA 0 slow path: retired slots
+};
+
+template <typename T>
+__device__ __forceinline__ T* cta0(cg::cluster_group& cl, T* p) {
+  return cl.map_shared_rank(p, 0);
+}
+
+template <int LPT>
+__global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
+    rerank_cluster_kernel(const RerankArgs a) {
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ RCShared sh;
+  extern __shared__ __align__(16) unsigned char rc_dyn[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rc_dyn);  // [K]
+  const int rank = static_cast<int>(cl.block_rank());
+  const int m = blockIdx.x / kRC;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = (a.ncand + kRC - 1) / kRC;
+  const int s0 = rank * chunk, s1 = min(a.ncand, s0 + chunk);
+  const float* cv = a.cand_val + static_cast<int64_t>(m) * a.ncand;
+  const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
+
+  // 1. keys and ids of this CTA's slots; x for the dots
+  uint32_t key[LPT], uid[LPT];
+#pragma unroll
+  for (int j = 0; j < LPT; ++j) {
+    const int i = s0 + tid + j * kRCThreads;
+    key[j] = i < s1 ? order_key(cv[i]) : 0u;
+    uid[j] = i < s1 ? static_cast<uint32_t>(ci[i]) ^ 0x80000000u : 0xffffffffu;
+  }
+  {
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
+    for (int i = tid; i < a.K / 8; i += kRCThreads) reinterpret_cast<uint4*>(xs)[i] = xr[i];
+  }
+  uint32_t tmax = 0u;
+#pragma unroll
+  for (int j = 0; j < LPT; ++j) tmax = max(tmax, key[j]);
+  tmax = __reduce_max_sync(0xffffffffu, tmax);
+  if (rank == 0 && tid == 0) sh.surv_n = 0;
+  if (lane == 0) cta0(cl, sh.allmax)[rank * kRCWarps + warp] = tmax;
+  cl.sync();
+
+  // 2. T: the R-th largest warp maximum (rank of each value by counting, ties by position)
+  if (rank == 0 && warp == 0) {
+    const uint32_t v0 = sh.allmax[lane], v1 = sh.allmax[32 + lane];
+    int r0 = 0, r1 = 0;
+    for (int src = 0; src < 32; ++src) {
+      const uint32_t o0 = __shfl_sync(0xffffffffu, v0, src);
+      const uint32_t o1 = __shfl_sync(0xffffffffu, v1, src);
+      r0 += (o0 > v0 || (o0 == v0 && src < lane)) + (o1 > v0);
+      r1 += (o0 >= v1) + (o1 > v1 || (o1 == v1 && src < lane));
+    }
+    const uint32_t T = __reduce_max_sync(
+        0xffffffffu, max(r0 == a.R - 1 ? v0 : 0u, r1 == a.R - 1 ? v1 : 0u));
+    if (lane < kRC) cl.map_shared_rank(&sh.T, lane)[0] = T;
+  }
+  cl.sync();
+
+  // 3. survivors (key >= T) into CTA 0's list
+  {
+    const uint32_t T = sh.T;
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < LPT; ++j) cnt += (key[j] != 0u && key[j] >= T) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sh.wcnt[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < kRCWarps; ++w) tot += sh.wcnt[w];
+      sh.base = tot ? atomicAdd(cta0(cl, &sh.surv_n), tot) : 0;
+    }
+    __syncthreads();
+    int pos = sh.base + incl - cnt;
+    for (int w = 0; w < warp; ++w) pos += sh.wcnt[w];
+    Sel* surv0 = cta0(cl, sh.surv);
+#pragma unroll
+    for (int j = 0; j < LPT; ++j)
+      if (key[j] != 0u && key[j] >= T) {
+        if (pos < kRCSurvCap)
+          surv0[pos] = Sel{key[j], uid[j], static_cast<uint32_t>(s0 + tid + j * kRCThreads)};
+        ++pos;
+      }
+  }
+  cl.sync();
+
+  // 4. CTA 0 selects the R first in selection order and sends the ids to every CTA
+  if (rank == 0) {
+    const int total = sh.surv_n;
+    if (total <= kRCSurvCap) {
+      if (warp == 0) {
+        if (total <= 32) {
+          Sel v = lane < total ? sh.surv[lane] : Sel{0u, 0xffffffffu, 0xffffffffu};
+          v = warp_sort(v);
+          if (lane < a.R) sh.rr[lane] = v.key ? static_cast<int32_t>(v.uid ^ 0x80000000u) : -1;
+        } else {
+          for (int r = 0; r < a.R; ++r) {
+            Sel best{0u, 0xffffffffu, 0xffffffffu};
+            for (int q = lane; q < total; q += 32) {
+              const Sel v = sh.surv[q];
+              if (v.key != 0u && (best.key == 0u || sel_before(v, best))) best = v;
+            }
+            const Sel wb = warp_best(best);
+            for (int q = lane; q < total; q += 32)
+              if (sh.surv[q].key != 0u && sh.surv[q].idx == wb.idx) sh.surv[q].key = 0u;
+            __syncwarp();
+            if (lane == 0) sh.rr[r] = wb.key ? static_cast<int32_t>(wb.uid ^ 0x80000000u) : -1;
+          }
+        }
+      }
+    } else {
+      // heavy ties overflowed the list: the exact R-round selection over the whole row
+      for (int i = tid; i < (a.ncand + 31) / 32; i += kRCThreads) sh.retired[i] = 0u;
+      __syncthreads();
+      for (int r = 0; r < a.R; ++r) {
+        Sel best{0u, 0xffffffffu, 0xffffffffu};
+        for (int i = tid; i < a.ncand; i += kRCThreads) {
+          if (sh.retired[i >> 5] & (1u << (i & 31))) continue;
+          const Sel v{order_key(cv[i]), static_cast<uint32_t>(ci[i]) ^ 0x80000000u,
+                      static_cast<uint32_t>(i)};
+          if (v.key != 0u && (best.key == 0u || sel_before(v, best))) best = v;
+        }
+        const Sel wb = warp_best(best);
+        if (lane == 0) sh.wbest[warp] = wb;
+        __syncthreads();
+        if (warp == 0) {
+          const Sel fb =
+              warp_best(lane < kRCWarps ? sh.wbest[lane] : Sel{0u, 0xffffffffu, 0xffffffffu});
+          if (lane == 0) {
+            sh.rr[r] = fb.key ? static_cast<int32_t>(fb.uid ^ 0x80000000u) : -1;
+            if (fb.key != 0u) sh.retired[fb.idx >> 5] |= 1u << (fb.idx & 31);
+          }
+        }
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+    if (tid < a.R) {
+      const int32_t id = sh.rr[tid];
+      a.rr_id[static_cast<int64_t>(m) * a.R + tid] = id;
+      for (int c = 1; c < kRC; ++c) cl.map_shared_rank(sh.rr, c)[tid] = id;
+    }
+  }
+  cl.sync();
+
+  // 5. exact dots of this CTA's slots (rank, rank + kRC, ...): all of a thread's weight loads
+  // for all its slots are in flight together; fixed-order reductions
+  {
+    const int nslot = (a.R - rank + kRC - 1) / kRC;  // 0..4
+    const int k8n = a.K / 8;
+    const uint4* xr = reinterpret_cast<const uint4*>(xs);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint4* wr[4];
+    bool live[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int n = u < nslot ? sh.rr[rank + u * kRC] : -1;
+      live[u] = n >= 0 && n < a.N;
+      wr[u] = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(live[u] ? n : 0) * a.K);
+    }
+    for (int k8b = tid; k8b < k8n; k8b += kRCThreads * 3) {
+      uint4 w8[4][3];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int k8 = k8b + q * kRCThreads;
+          w8[u][q] = live[u] && k8 < k8n ? ldg_nc_v4(wr[u] + k8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int k8 = k8b + q * kRCThreads;
+        if (k8 < k8n) {
+          const uint4 x8 = xr[k8];
+          const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t wv[4] = {w8[u][q].x, w8[u][q].y, w8[u][q].z, w8[u][q].w};
+            float p = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              p = fmaf(__uint_as_float(xv[e] << 16), __uint_as_float(wv[e] << 16), p);
+              p = fmaf(__uint_as_float(xv[e] & 0xffff0000u), __uint_as_float(wv[e] & 0xffff0000u), p);
+            }
+            acc[u] += p;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+      if (lane == 0) sh.part[u][warp] = acc[u];
+    }
+    __syncthreads();
+    if (tid < nslot) {
+      const int j = rank + tid * kRC;
+      const int n = sh.rr[j];
+      float v = -INFINITY;
+      if (n >= 0 && n < a.N) {
+        v = 0.0f;
+        for (int w = 0; w < kRCWarps; ++w) v += sh.part[tid][w];
+      } else if (n >= a.N) {
+        set_status(a.status, DH_DEV_BAD_ID);
+      }
+      cta0(cl, sh.logit)[j] = v;
+    }
+  }
+  cl.sync();
+
+  // 6. CTA 0: outputs and the argmax (ties to the lowest id)
+  if (rank == 0 && warp == 0) {
+    uint32_t bk = 0u, bu = 0xffffffffu;
+    for (int j = lane; j < a.R; j += 32) {
+      const float v = sh.logit[j];
+      const int32_t n = sh.rr[j];
+      a.rr_logit[static_cast<int64_t>(m) * a.R + j] = v;
+      if (a.y && n >= 0 && n < a.N)
+        a.y[static_cast<int64_t>(m) * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      const uint32_t k = order_key(v);
+      const uint32_t u = static_cast<uint32_t>(n) ^ 0x80000000u;
+      if (k > bk || (k == bk && u < bu)) {
+        bk = k;
+        bu = u;
+      }
+    }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t umin = __reduce_min_sync(0xffffffffu, bk == kmax ? bu : 0xffffffffu);
+    if (lane == 0) a.argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+  }
+}
+
+template <int LPT>
+static cudaError_t launch_rc(const RerankArgs& a, int M, cudaStream_t s) {
+  const int smem = 2 * a.K;
+  cudaError_t e = cudaFuncSetAttribute(rerank_cluster_kernel<LPT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  rerank_cluster_kernel<LPT><<<M * kRC, kRCThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int LPT>
 static cudaError_t launch_rr(const RerankArgs& a, int M, cudaStream_t s) {
   size_t smem = static_cast<size_t>(2 * a.K) + sizeof(Sel) * (kRerankWarps + 1) +
@@ -361,6 +644,13 @@ cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s) {
   a.y = static_cast<uint16_t*>(rc.y);
   a.status = rc.status;
   const int M = static_cast<int>(rc.M);
+  if (rc.R <= kRCMaxR && rc.ncand <= kRCMaxCand && rc.K <= 32768) {
+    const int64_t lpt = ((rc.ncand + kRC - 1) / kRC + kRCThreads - 1) / kRCThreads;
+    if (lpt <= 1) return launch_rc<1>(a, M, s);
+    if (lpt <= 2) return launch_rc<2>(a, M, s);
+    if (lpt <= 4) return launch_rc<4>(a, M, s);
+    return launch_rc<8>(a, M, s);
+  }
   const int64_t per = (rc.ncand + kRerankThreads - 1) / kRerankThreads;
   if (per <= 1) return launch_rr<1>(a, M, s);
   if (per <= 2) return launch_rr<2>(a, M, s);

@@ -103,7 +103,9 @@ def test_coarse_topk_parity(M, K, N, G, bits, kcand, seed):
 
 def _rand_candidates(rng, M, ncand, N, tie_levels=None):
     val = rng.standard_normal((M, ncand)).astype(np.float32)
-    if tie_levels:
+    if tie_levels == "const":
+        val[:] = 0.5                      # every candidate ties: the exact slow selection
+    elif tie_levels:
         val = (np.round(val * tie_levels) / tie_levels).astype(np.float32)
     ids = np.stack([rng.choice(N, ncand, replace=False) for _ in range(M)]).astype(np.int32)
     return val, ids
@@ -117,6 +119,11 @@ RERANK_CASES = [
     (2, 1024, 8192, 64, 64, 2, 33),         # R = ncand
     (5, 5120, 4096, 300, 1, None, 34),      # R = 1
     (2, 1024, 8192, 3000, 256, None, 35),   # R = 256
+    # the cluster path (R <= 32, ncand <= 16384)
+    (8, 5120, 20000, 15520, 16, None, 36),  # the page's candidate count and R
+    (2, 1024, 20000, 16384, 32, None, 37),  # largest cluster case
+    (3, 2048, 8192, 2000, 17, 8, 38),       # R not a multiple of the cluster size, ties
+    (2, 1024, 8192, 3000, 16, "const", 39),  # all values tie: survivor list overflows
 ]
 
 
