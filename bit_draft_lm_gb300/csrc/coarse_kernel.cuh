@@ -41,11 +41,12 @@
 //    -XS split exactly into three bf16 parts (hi, mid, lo), fp32 accumulation. The first warp to
 //    finish a block runs it for the block's four tiles and writes it to an extra partial slot,
 //    so the per-tile loop has no zero-point work and no per-tile branch.
-//  * One hidden row (M = 1): the MMA's 8 columns would be 7/8 idle, so each scale group of the
-//    strip gets its own column instead. Lane column g of the B operand holds x for the planes of
-//    scale group g and zeros elsewhere, so one accumulator collects every plane of the tile, each
-//    in its own column, and the per-group scale is applied once per tile per group (lanes
-//    c = 0, 1 hold columns 0..3), not once per plane per accumulator register.
+//  * One hidden row (M = 1): the MMA's 8 columns would be 7/8 idle, so each scale group q of the
+//    strip gets its own column q. The lanes of B column g hold the x values of their own group
+//    g only (8 registers instead of 32), every MMA of group q accumulates into its own
+//    accumulator, and only column q of that accumulator is read (the others pair group q's
+//    weights with another group's x and are ignored). The per-group scale is then applied once
+//    per tile per group (lanes c = 0, 1 hold columns 0..3).
 //  * The per-group scale is applied to the accumulator, never to the weight tile.
 // Hidden rows are processed eight at a time (one MMA column tile); M > 8 runs ceil(M/8) passes.
 #pragma once
@@ -211,18 +212,40 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   const uint32_t dst_lane =
       smem_addr(sm + a.off_ring + warp * (NSW * WSTAGE)) + r0l * SB + 16 * pcol0;
   const int src_lane = strip_byte + 16 * col0;
-  // tile tk of local block lbk into ring stage (4 lbk + tk) % NSW. Past this CTA's blocks the
-  // copies read nothing (zero-fill); rows past N re-read row N - 1 (their values are ignored).
-  auto load_tile = [&](int lbk, int tk) {
-    const bool live = lbk < my_blocks;
-    const int row = block_row0(lbk) + tk * kTileRows + r0l;
-    const uint32_t dst = dst_lane + ((4 * lbk + tk) & (NSW - 1)) * WSTAGE;
+  // Weight prefetch. blk_src(lbk): this lane's source pointer for local block lbk (row r0l of
+  // the block), whether the block is one of this CTA's and whether it lies below N; computed
+  // once per block, so a tile's copies use compile-time offsets from it. Past this CTA's blocks
+  // the copies read nothing (zero-fill); in the block that crosses N, rows past N re-read row
+  // N - 1 (their values are ignored).
+  struct BlkSrc {
+    const uint8_t* p;
+    int row0;
+    bool live, full;
+  };
+  auto blk_src = [&](int lbk) {
+    BlkSrc b;
+    b.row0 = block_row0(lbk);
+    b.live = lbk < my_blocks;
+    b.full = b.row0 + kBlockRows <= a.N;
+    b.p = a.packed + static_cast<int64_t>(b.row0 + r0l) * RB + src_lane;
+    return b;
+  };
+  // ring stage of tile tk of local block lbk: (4 lbk + tk) mod NSW
+  auto ring_stage = [&](int lbk, int tk) { return (((4 * lbk) & (NSW - 1)) + tk) & (NSW - 1); };
+  auto load_tile = [&](const BlkSrc& b, int lbk, int tk) {
+    const uint32_t dst = dst_lane + ring_stage(lbk, tk) * WSTAGE;
+    if (b.live && b.full) {
 #pragma unroll
-    for (int j = 0; j < CH; ++j) {
-      const int rj = min(row + j * RPJ, a.N - 1);
-      cp_async16(dst + j * RPJ * SB, live ? a.packed + static_cast<int64_t>(rj) * RB + src_lane
-                                          : a.packed,
-                 live);
+      for (int j = 0; j < CH; ++j)
+        cp_async16(dst + j * RPJ * SB, b.p + static_cast<int64_t>(tk * kTileRows + j * RPJ) * RB,
+                   true);
+    } else {
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int rj = min(b.row0 + tk * kTileRows + r0l + j * RPJ, a.N - 1);
+        cp_async16(dst + j * RPJ * SB,
+                   b.live ? a.packed + static_cast<int64_t>(rj) * RB + src_lane : a.packed, b.live);
+      }
     }
     cp_async_commit();  // one group per tile slot, possibly empty, keeps the counting uniform
   };
@@ -243,8 +266,12 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
                                  xg + p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i)
                            : make_uint2(0u, 0u);
 
+  {
+    const BlkSrc b0 = blk_src(0), b1 = blk_src(1);
 #pragma unroll
-  for (int t = 0; t < NSW - 1; ++t) load_tile(t / kTilesPerBlock, t % kTilesPerBlock);
+    for (int t = 0; t < NSW - 1; ++t)
+      load_tile(t / kTilesPerBlock ? b1 : b0, t / kTilesPerBlock, t % kTilesPerBlock);
+  }
 
   // S column of scale group q = (fold segment f, plane p) of this strip: p*(RB/G) + (strip+64f)/G
   auto s_col = [&](int q) {
@@ -256,9 +283,15 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   // and {1, 3} (register 1), plane p, as f16 x * s / 2^plane_shift(p). Each warp scales by its
   // own power of two s = 2^(15 - E), max |x| = f * 2^E (f in [0.5, 1)) over its strip of the
   // row, and converts its partials to logit units before storing them. With one hidden row,
-  // column g keeps only the values of scale group q = g (zeros elsewhere). Also the sums of x
+  // scale group q has MMA column q: the lanes of column g hold only the values of their own group
+  // q = g (lanes g >= NQ hold group 0's, their columns are never read), and every MMA takes the
+  // lane's own values: column q of the accumulator of group q is then exact. Also the sums of x
   // over the strip's part of each scale group q.
-  uint32_t bfr[U][4][P][2];
+  constexpr int BU = MT1 ? (SPLIT ? 1 : U) : U;  // B registers: [BU][4][BP][2]
+  constexpr int BP = MT1 ? 1 : P;
+  uint32_t bfr[BU][4][BP][2];
+  const int q_own = MT1 && g < NQ ? g : 0;  // MT1: this lane's scale group
+  const int u_own = SPLIT ? q_own / P : 0, p_own = q_own % P;
   int ew;  // E of this warp's strip of the lane's hidden row
   float xsg[NQ];
   {
@@ -287,6 +320,12 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     ew = static_cast<int>(mx >> 7) - 126;
     ew = ew < -100 ? -100 : (ew > 100 ? 100 : ew);  // zero or tiny rows
 #pragma unroll
+    for (int u = 0; u < BU; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) bfr[u][i][0][e] = 0u;
+#pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -299,9 +338,17 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             hs[e] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(h[e]) * sx));
-          const bool keep = !MT1 || ((SPLIT ? u * P : 0) + p) == g;
-          bfr[u][i][p][0] = keep ? hs[0] | (hs[2] << 16) : 0u;  // (x[k0], x[k0+2]): even bytes
-          bfr[u][i][p][1] = keep ? hs[1] | (hs[3] << 16) : 0u;  // (x[k0+1], x[k0+3]): odd bytes
+          const uint32_t r0 = hs[0] | (hs[2] << 16);  // (x[k0], x[k0+2]): even bytes of the word
+          const uint32_t r1 = hs[1] | (hs[3] << 16);  // (x[k0+1], x[k0+3]): odd bytes
+          if (MT1) {
+            if (p == p_own && (!SPLIT || u == u_own)) {
+              bfr[SPLIT ? 0 : u][i][0][0] = r0;
+              bfr[SPLIT ? 0 : u][i][0][1] = r1;
+            }
+          } else {
+            bfr[u][i][MT1 ? 0 : p][0] = r0;
+            bfr[u][i][MT1 ? 0 : p][1] = r1;
+          }
         }
   }
   // Group sums XS[m][col] of the whole row (for the zero-point MMA): each warp publishes its
@@ -311,6 +358,9 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     for (int q = 0; q < NQ; ++q) xs_part[(warp * 8 + g) * NQ + q] = xsg[q];
   }
   __syncthreads();  // barriers initialised, strip sums published
+  // a dependent kernel (the rerank) may be scheduled as SMs free up; it waits for this grid's
+  // completion before it reads anything this kernel writes
+  if (threadIdx.x == 0) grid_launch_dependents();
   {
     const int RBG = RB / G;  // groups per plane
     for (int e = threadIdx.x; e < mt * KG; e += blockDim.x) {
@@ -558,18 +608,26 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     }
     const unsigned char* stage = sz + sst * 2 * sz_half;
     float* rwb = rw_base + buf * (NW + 1) * red_wstride;
+    // the prefetches of this block's tiles target blocks lb + kA and lb + kA + 1
+    constexpr int kA = (NSW - 1) / kTilesPerBlock;
+    const BlkSrc bA = blk_src(lb + kA), bB = blk_src(lb + kA + 1);
 #pragma unroll
     for (int t = 0; t < kTilesPerBlock; ++t) {
-      constexpr int kAhead = NSW - 1;
-      load_tile(lb + (t + kAhead) / kTilesPerBlock, (t + kAhead) % kTilesPerBlock);
+      {
+        const int pt = t + NSW - 1, pb = pt / kTilesPerBlock - kA, ptk = pt % kTilesPerBlock;
+        load_tile(pb ? bB : bA, lb + kA + pb, ptk);
+      }
       cp_async_wait<NSW - 1>();  // tile (lb, t) has landed (for this lane's copies)
       __syncwarp();              // ... and for every lane's
-      const unsigned char* cs = ring + ((kTilesPerBlock * lb + t) & (NSW - 1)) * WSTAGE;
+      const unsigned char* cs = ring + ring_stage(lb, t) * WSTAGE;
       const unsigned char* szs = stage + t * (kTileRows * KG * 2);
       float acc[4];
       if (MT1) {
-        // every plane of the tile into one accumulator (scale group q in column q), two chains
-        float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // one accumulator per scale group q (four independent chains); column q of dq[q] is
+        // group q's dot, the other columns are ignored
+        float dq[NQ][4];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) dq[q][0] = dq[q][1] = dq[q][2] = dq[q][3] = 0.0f;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int pc = BITS == 4 ? ((4 * u + c) ^ ((g & 1) << 2)) : c;  // swizzled column
@@ -581,18 +639,32 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
             const uint32_t tao = ta[i] >> 8, tbo = tb[i] >> 8;
 #pragma unroll
             for (int p = 0; p < P; ++p)
-              mma_f16_16816_acc((i & 1) ? d1 : d0, dq16<BITS>(ta[i], p), dq16<BITS>(tb[i], p),
-                                dq16<BITS>(tao, p), dq16<BITS>(tbo, p), bfr[u][i][p][0],
-                                bfr[u][i][p][1]);
+              mma_f16_16816_acc(dq[(SPLIT ? u * P : 0) + p], dq16<BITS>(ta[i], p),
+                                dq16<BITS>(tb[i], p), dq16<BITS>(tao, p), dq16<BITS>(tbo, p),
+                                bfr[SPLIT ? 0 : u][i][0][0], bfr[SPLIT ? 0 : u][i][0][1]);
           }
         }
-        // d: (row g, group 2c), (row g, group 2c+1), (row g+8, group 2c), (row g+8, group 2c+1)
+        // lane c holds columns 2c, 2c + 1: group 2c in dq[2c][0, 2], group 2c + 1 in
+        // dq[2c + 1][1, 3] (rows g, g + 8)
+        float da0, da2, db1, db3;
+        if (NQ > 2) {
+          const bool hi = c & 1;  // lanes c = 2, 3 only pair with each other below
+          da0 = hi ? dq[NQ > 2 ? 2 : 0][0] : dq[0][0];
+          da2 = hi ? dq[NQ > 2 ? 2 : 0][2] : dq[0][2];
+          db1 = hi ? dq[NQ > 3 ? 3 : 1][1] : dq[1][1];
+          db3 = hi ? dq[NQ > 3 ? 3 : 1][3] : dq[1][3];
+        } else {
+          da0 = dq[0][0];
+          da2 = dq[0][2];
+          db1 = dq[NQ > 1 ? 1 : 0][1];
+          db3 = dq[NQ > 1 ? 1 : 0][3];
+        }
         const float sa = __uint_as_float(lds_u16(szs + soa) * a.u16_mul);
         const float sb = __uint_as_float(lds_u16(szs + sob) * a.u16_mul);
         const float sa8 = __uint_as_float(lds_u16(szs + soa + row8) * a.u16_mul);
         const float sb8 = __uint_as_float(lds_u16(szs + sob + row8) * a.u16_mul);
-        float r0 = fmaf(sb, d0[1] + d1[1], sa * (d0[0] + d1[0]));
-        float r8 = fmaf(sb8, d0[3] + d1[3], sa8 * (d0[2] + d1[2]));
+        float r0 = fmaf(sb, db1, sa * da0);
+        float r8 = fmaf(sb8, db3, sa8 * da2);
         if (NQ > 2) {  // groups 2, 3 sit in lane c = 1
           r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
           r8 += __shfl_xor_sync(0xffffffffu, r8, 1);
@@ -627,8 +699,8 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma_f16_16816_acc(d[p], dq16<BITS>(ta[i], p), dq16<BITS>(tb[i], p),
-                                dq16<BITS>(tao[i], p), dq16<BITS>(tbo[i], p), bfr[u][i][p][0],
-                                bfr[u][i][p][1]);
+                                dq16<BITS>(tao[i], p), dq16<BITS>(tbo[i], p),
+                                bfr[u][i][MT1 ? 0 : p][0], bfr[u][i][MT1 ? 0 : p][1]);
             if (seg_last) {
               const unsigned char* sq = szs + so_g + 2 * s_col(f * P + p);
               const float sg = __uint_as_float(lds_u16(sq) * a.u16_mul);
@@ -679,8 +751,15 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
       }
     }
   }
-  // drain: take epilogue jobs until every job of this CTA has been taken by some warp
-  {
+  // drain. One job per block: take the jobs that are ready, then leave (every block's jobs are
+  // published by a warp before it drains, so the warp that publishes the last block takes
+  // whatever is left).
+  if (MT1) {
+    while (try_job(true)) {
+    }
+  } else {
+    // several jobs per block: wait (sleeping) for the rest, so the last blocks' jobs run in
+    // parallel on the warps that are done rather than one after another on the last publisher
     const uint64_t t0 = global_timer_ns();
     while (true) {
       int st = 0;
@@ -688,7 +767,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
         st = *reinterpret_cast<volatile int*>(jobs_claimed) >= my_blocks * mt || *abort_flag;
       if (__shfl_sync(0xffffffffu, st, 0)) break;
       if (try_job(true)) continue;
-      __nanosleep(128);
+      __nanosleep(1000);
       if (lane == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
         set_status(a.status, DH_DEV_WAIT_TIMEOUT);

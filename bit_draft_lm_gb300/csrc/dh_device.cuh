@@ -191,6 +191,16 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t
                : "r"(smem_addr(row_addr)));
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization waits
+// here until the preceding kernel in the stream has completed and its writes are visible (a
+// no-op for a normal launch); a preceding kernel lets its dependents start early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

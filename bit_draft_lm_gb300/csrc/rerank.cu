@@ -388,17 +388,20 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
   const float* cv = a.cand_val + static_cast<int64_t>(m) * a.ncand;
   const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
 
-  // 1. keys and ids of this CTA's slots; x for the dots
+  // 1. x for the dots (an input of the call, not of the previous kernel: staged before the
+  // wait), then, once the kernel that wrote the candidates has completed (programmatic
+  // dependent launch; a no-op otherwise), the keys and ids of this CTA's slots
+  {
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
+    for (int i = tid; i < a.K / 8; i += kRCThreads) reinterpret_cast<uint4*>(xs)[i] = xr[i];
+  }
+  grid_dependency_wait();
   uint32_t key[LPT], uid[LPT];
 #pragma unroll
   for (int j = 0; j < LPT; ++j) {
     const int i = s0 + tid + j * kRCThreads;
     key[j] = i < s1 ? order_key(cv[i]) : 0u;
     uid[j] = i < s1 ? static_cast<uint32_t>(ci[i]) ^ 0x80000000u : 0xffffffffu;
-  }
-  {
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
-    for (int i = tid; i < a.K / 8; i += kRCThreads) reinterpret_cast<uint4*>(xs)[i] = xr[i];
   }
   uint32_t tmax = 0u;
 #pragma unroll
@@ -610,7 +613,20 @@ static cudaError_t launch_rc(const RerankArgs& a, int M, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(rerank_cluster_kernel<LPT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  rerank_cluster_kernel<LPT><<<M * kRC, kRCThreads, smem, s>>>(a);
+  // programmatic dependent launch: the CTAs may start (and stage x) while the kernel before
+  // them in the stream finishes; they wait for its completion before reading the candidates
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M * kRC);
+  cfg.blockDim = dim3(kRCThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, rerank_cluster_kernel<LPT>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
