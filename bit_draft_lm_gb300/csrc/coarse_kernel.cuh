@@ -249,9 +249,23 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     }
     cp_async_commit();  // one group per tile slot, possibly empty, keeps the counting uniform
   };
-  // ---- this warp's view of x, loaded before the weight prefetch so that it does not queue
-  // behind it: the strip's values for the MMA's B operand. Lanes of column g hold hidden row g
-  // (zeros for g >= mt); with one hidden row every lane holds it.
+  // ---- weight prefetch: the first NSW - 1 tiles of this warp's strip (and, above, the S/ZS
+  // stages). The weights are not an output of the kernel that precedes this one in the stream
+  // when that kernel lets its dependents start early (this library's rerank and coarse
+  // kernels), so they are read before the wait below; a kernel that does not trigger early has
+  // completed before this one starts.
+  {
+    const BlkSrc b0 = blk_src(0), b1 = blk_src(1);
+#pragma unroll
+    for (int t = 0; t < NSW - 1; ++t)
+      load_tile(t / kTilesPerBlock ? b1 : b0, t / kTilesPerBlock, t % kTilesPerBlock);
+  }
+  // Launched as a programmatic dependent: everything below (x, the outputs) waits for the
+  // preceding kernel's completion (a no-op after an ordinary launch).
+  grid_dependency_wait();
+
+  // ---- this warp's view of x: the strip's values for the MMA's B operand. Lanes of column g
+  // hold hidden row g (zeros for g >= mt); with one hidden row every lane holds it.
   const int xrow = MT1 ? 0 : (g < mt ? g : 0);
   const bool xval = MT1 || g < mt;
   const uint16_t* xg = a.x + static_cast<int64_t>(a.m0 + xrow) * K;
@@ -265,13 +279,6 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
         xv[u][i][p] = xval ? *reinterpret_cast<const uint2*>(
                                  xg + p * (K / P) + strip_byte + 64 * u + 16 * c + 4 * i)
                            : make_uint2(0u, 0u);
-
-  {
-    const BlkSrc b0 = blk_src(0), b1 = blk_src(1);
-#pragma unroll
-    for (int t = 0; t < NSW - 1; ++t)
-      load_tile(t / kTilesPerBlock ? b1 : b0, t / kTilesPerBlock, t % kTilesPerBlock);
-  }
 
   // S column of scale group q = (fold segment f, plane p) of this strip: p*(RB/G) + (strip+64f)/G
   auto s_col = [&](int q) {
@@ -794,7 +801,20 @@ cudaError_t launch_coarse_variant(const CoarseArgs& a, int nsw, int grid, cudaSt
     const int smem = a.off_ring + a.NW * nsw * kTileRows * SB;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, a.NW * 32, smem, s>>>(a);
+    // programmatic dependent launch: the CTAs may start (and prefetch weights) while the kernel
+    // before them in the stream finishes, once it lets its dependents start
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(a.NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
   auto by_nsw = [&](auto kspec, auto mt1) -> cudaError_t {

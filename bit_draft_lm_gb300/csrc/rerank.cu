@@ -113,6 +113,9 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
   const int m = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint16_t* xrow = a.x + static_cast<int64_t>(m) * a.K;
+  // the next kernel in the stream (the next call's coarse pass) may start its weight prefetch
+  // on the SMs this small grid leaves idle; it waits for this grid before reading anything else
+  if (tid == 0) grid_launch_dependents();
 
   const float* cv = a.cand_val + static_cast<int64_t>(m) * a.ncand;
   const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
@@ -387,6 +390,9 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
   const int s0 = rank * chunk, s1 = min(a.ncand, s0 + chunk);
   const float* cv = a.cand_val + static_cast<int64_t>(m) * a.ncand;
   const int32_t* ci = a.cand_id + static_cast<int64_t>(m) * a.ncand;
+  // the next kernel in the stream (the next call's coarse pass) may start its weight prefetch
+  // on the SMs this small grid leaves idle; it waits for this grid before reading anything else
+  if (tid == 0) grid_launch_dependents();
 
   // 1. x for the dots (an input of the call, not of the previous kernel: staged before the
   // wait), then, once the kernel that wrote the candidates has completed (programmatic
