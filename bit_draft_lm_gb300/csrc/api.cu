@@ -92,17 +92,18 @@ int quantize(int bits, const void* W, int64_t N, int64_t K, int G, uint8_t* pack
   return ok();
 }
 
-size_t workspace_bytes_impl(int64_t M) {
-  (void)M;
-  return kWorkspaceHeader;
+// The rerank needs the status word only; the coarse pass of more than kWideMinRows hidden rows
+// also keeps its scratch after the header.
+size_t rerank_workspace_bytes() { return kWorkspaceHeader; }
+size_t coarse_workspace_bytes(int64_t M, int64_t K) {
+  return kWorkspaceHeader + dh::coarse_wide_scratch_bytes(M, K);
 }
 
-int check_workspace(void* ws, size_t ws_bytes, int64_t M, const char* who) {
+int check_workspace(void* ws, size_t ws_bytes, size_t need, const char* who) {
   if (!ws) return fail(DH_ERR_WORKSPACE, "%s: workspace is NULL", who);
   if (!aligned(ws, 256)) return fail(DH_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", who);
-  if (ws_bytes < workspace_bytes_impl(M))
-    return fail(DH_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required", who, ws_bytes,
-                workspace_bytes_impl(M));
+  if (ws_bytes < need)
+    return fail(DH_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required", who, ws_bytes, need);
   return DH_OK;
 }
 
@@ -112,6 +113,8 @@ namespace dh {
 // Records `msg` as the calling thread's dh_last_error() message and returns `code` (for entry
 // points defined in other files of the library).
 int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
+// Workspace bytes the rerank entry point requires (the status word's header).
+size_t rerank_workspace_needed() { return rerank_workspace_bytes(); }
 }  // namespace dh
 
 extern "C" {
@@ -136,11 +139,11 @@ size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits) {
 
 size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank) {
   (void)N;
-  (void)K;
   (void)kcand;
   (void)rerank;
-  if (M < 1) return 0;
-  return workspace_bytes_impl(M);
+  if (M < 1 || K < 1) return 0;
+  const size_t c = coarse_workspace_bytes(M, K), r = rerank_workspace_bytes();
+  return c > r ? c : r;
 }
 
 int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
@@ -168,13 +171,17 @@ int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t
     return fail(DH_ERR_ALIGN, "%s: x, packed, S and ZS must be 16-byte aligned", who);
   if (!aligned(cand_val, 4) || !aligned(cand_id, 4) || (y_coarse && !aligned(y_coarse, 2)))
     return fail(DH_ERR_ALIGN, "%s: output misaligned", who);
-  int rc = check_workspace(workspace, ws_bytes, M, who);
+  int rc = check_workspace(workspace, ws_bytes, coarse_workspace_bytes(M, K), who);
   if (rc != DH_OK) return rc;
   DeviceInfo di;
   cudaError_t e = device_info(di);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
-  dh::CoarseCall cc{x, M, K, packed, S, ZS, N, G, bits, kcand, cand_val, cand_id, y_coarse,
-                    static_cast<uint32_t*>(workspace)};
+  void* scratch = dh::coarse_wide_scratch_bytes(M, K)
+                      ? static_cast<unsigned char*>(workspace) + kWorkspaceHeader
+                      : nullptr;
+  dh::CoarseCall cc{x,        M,       K,       packed,   S,
+                    ZS,       N,       G,       bits,     kcand,
+                    cand_val, cand_id, y_coarse, static_cast<uint32_t*>(workspace), scratch};
   e = dh::launch_coarse_topk(cc, di.sms, di.max_smem, reinterpret_cast<cudaStream_t>(s));
   if (e == cudaErrorInvalidValue)
     return fail(DH_ERR_SHAPE, "%s: shape does not fit the kernel's shared-memory plan", who);
@@ -204,7 +211,7 @@ int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void*
   if (!aligned(cand_val, 4) || !aligned(cand_id, 4) || !aligned(rr_id, 4) ||
       !aligned(rr_logit, 4) || !aligned(argmax_id, 4) || (y_coarse && !aligned(y_coarse, 2)))
     return fail(DH_ERR_ALIGN, "%s: misaligned candidate or output array", who);
-  int rc = check_workspace(workspace, ws_bytes, M, who);
+  int rc = check_workspace(workspace, ws_bytes, rerank_workspace_bytes(), who);
   if (rc != DH_OK) return rc;
   dh::RerankCall r{x, M, K, W, N, cand_val, cand_id, ncand, rerank, rr_id, rr_logit, argmax_id,
                    y_coarse, static_cast<uint32_t*>(workspace)};

@@ -53,6 +53,9 @@ static int plan_coarse(CoarseArgs& a, int max_smem, int nsw_max) {
 
 // Returns cudaErrorInvalidValue if the shape does not fit the kernel's plan.
 cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s) {
+  // many hidden rows of an int2 head: one tensor-core pass instead of several warp-MMA passes
+  if (cc.scratch != nullptr && coarse_wide_supports(cc))
+    return launch_coarse_wide(cc, cc.scratch, num_sms, max_smem, s);
   CoarseArgs a{};
   a.x = static_cast<const uint16_t*>(cc.x);
   a.M = static_cast<int>(cc.M);

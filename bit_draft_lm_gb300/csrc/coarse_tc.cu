@@ -1,0 +1,700 @@
+// Coarse pass + block top-KCAND of the int2 draft head for many hidden rows at once (page
+// "radiance_drafthead.py": module docstring, _draft_head_int2 and _emit), on the
+// 5th-generation tensor cores of sm_103a: tcgen05.mma with the dequantised weights in tensor
+// memory (TMEM) and the hidden states in shared memory.
+//
+// Why only for many hidden rows: measured on GB300, one tcgen05.mma kind::f16 with M = 128,
+// K = 16 occupies the tensor pipe for ~95 ns whatever N (16 .. 256) and wherever A comes from.
+// Covering the vocabulary-scale head (124160 rows x 5120 codes) takes 310,400 such
+// instructions, ~193 us on 152 SMs, for any number of hidden rows up to 256; the warp-level
+// mma.sync kernel (coarse_kernel.cuh) takes 1/11 of that time per 16 x 16 tile step and wins
+// while the hidden rows fit a few of its passes. Here one pass takes up to 80 hidden rows.
+//
+// Work decomposition:
+//  * A prep kernel lays the pass's hidden states out as the MMA's B operand in the caller's
+//    workspace: x * 2^(15 - E_m) / 4^p as f16 (E_m from max |x[m]|; plane p's codes are
+//    v * 4^p * 2^-24 as f16 subnormals, so every product is v x 2^(15 - E_m) 2^-24 exactly),
+//    grouped per (scale group J, plane p) into one contiguous unit; also the group sums XS.
+//  * Persistent grid, one CTA per SM, 128-row tiles (the MMA's M = TMEM lanes). Warp 0 streams
+//    the packed rows through a ring of 128 x 128-byte stages with 2-D tensor-map copies (TMA,
+//    128-byte swizzle); warp 2 streams the B units through a second ring with bulk copies.
+//  * 4 dequantising warps: the thread of TMEM lane r owns row r. A 16-byte chunk of its row
+//    (16 byte positions x 4 planes) becomes 32 registers of f16 pairs with one AND each (the
+//    odd bytes come down by one shift per word), written to a TMEM A stage by one tcgen05.st;
+//    plane p's 16 codes are the stage's columns 8p .. 8p + 7.
+//  * Warp 1 (one thread) issues the MMAs plane by plane within each scale group: for plane p,
+//    the group's chunks accumulate into one D slot (128 x N fp32), which is then handed to the
+//    fold warps while the next plane accumulates into the other slot. So the page's
+//    per-group scale is applied to the accumulator, never to the weight tile:
+//    acc += S[n, g] * D_g. The zero-point part sum_g (S - ZS) XS_g (the page's
+//    S (XS + sum x v / 4) - ZS XS rearranged) is a per-row dot with the group sums.
+//  * 8 fold warps (two per TMEM lane quadrant, half of the columns each; thread = row) add
+//    S_g D_g and the zero-point part (S_g - ZS_g) XS_g of every slot into registers, then hand
+//    the tile's keys to 4 selection warps, which pick the top-KCAND of each 64-row block per
+//    hidden row (warp reductions on order-preserving keys, lowest row on ties).
+// Every wait is bounded (kWaitLimitNs); a wait that runs out marks the launch failed in the
+// status word, after which every wait returns at once and the kernel runs to its end.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "dh_device.cuh"
+#include "dh_launch.h"
+#include "tc_device.cuh"
+
+namespace dh {
+
+constexpr int kWRows = 128;        // vocab rows per tile (MMA M, TMEM lanes)
+constexpr int kWStageBytes = 128;  // packed bytes of a row per ring stage (8 chunks)
+constexpr int kWStageSmem = kWRows * kWStageBytes;
+constexpr int kWWarps = 19;  // producer, MMA, B producer, 4 dequantising, 8 fold, 4 selection
+constexpr int kWThreads = kWWarps * 32;
+constexpr int kWMaxNP = 8;  // packed ring stages at most
+constexpr int kWMaxNB = 4;  // B ring units at most
+constexpr int kWMaxNA = 12;
+constexpr int kWTmemCols = 512;
+constexpr int kWPrepThreads = 256;
+
+struct WideArgs {
+  int R;  // hidden rows of this pass (<= the MMA's N)
+  int K, N, RB, KG, NJ, NC, NS, ntiles;
+  const uint16_t* S;   // bf16 [N, KG]
+  const uint16_t* ZS;  // bf16 [N, KG]
+  const unsigned char* bbuf;  // B units [NJ][4][CPJ][2][NCOL][16 bytes] (prep)
+  const float* xs;            // [NCOL][KG] group sums of x (prep)
+  const int* ew;              // [NCOL] E_m (prep)
+  int m0;                     // first hidden row of the pass (outputs)
+  int kcand, nblk;
+  float* cand_val;  // [M, nblk * kcand]
+  int32_t* cand_id;
+  uint16_t* y;  // bf16 [M, N] or nullptr
+  uint32_t* status;
+  int np, nbu, unit_bytes, szp;
+  int off_bring, off_sz, off_keys, off_xs, off_ew, off_bars;
+};
+
+__device__ __forceinline__ void w_cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ float w_pow2(int e) {
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// ---- prep: one CTA per MMA column m (hidden row m0 + m of the pass; zeros past R) -------------
+template <int G>
+__global__ void __launch_bounds__(kWPrepThreads) wide_prep_kernel(const uint16_t* x, int m0,
+                                                                  int R, int K, int ncol,
+                                                                  unsigned char* bbuf, float* xs,
+                                                                  int* ew) {
+  // x may be an output of the preceding kernel, and the buffers may still be read by it (the
+  // previous pass): wait for its completion before anything else
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  constexpr int CPJ = G / 16;
+  __shared__ uint32_t red[kWPrepThreads / 32];
+  const int m = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool live = m < R;
+  const int RB = K / 4, KG = K / G;
+  const uint16_t* xr = x + static_cast<int64_t>(m0 + (live ? m : 0)) * K;
+  uint32_t mx = 0u;  // max |x| as bf16 magnitude bits
+  if (live) {
+    for (int i = tid; i < K / 8; i += kWPrepThreads) {
+      const uint4 v = reinterpret_cast<const uint4*>(xr)[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = 0u;
+#pragma unroll
+  for (int i = 0; i < kWPrepThreads / 32; ++i) mx = max(mx, red[i]);
+  int e = static_cast<int>(mx >> 7) - 126;  // max |x| = f 2^e, f in [0.5, 1)
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  if (tid == 0) ew[m] = live ? e : 0;
+  // item it = ((J * 4 + p) * CPJ + cj) * 2 + h: the 8 values of K-half h of chunk c = J CPJ + cj
+  // of plane p, in the order of the A columns (bytes 0, 2, 1, 3 of each word)
+  for (int it = tid; it < K / 8; it += kWPrepThreads) {
+    const int h = it & 1, t = it >> 1, cj = t % CPJ, t2 = t / CPJ, p = t2 & 3, J = t2 >> 2;
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (live) {
+      const int k0 = p * RB + 16 * (J * CPJ + cj) + 8 * h;
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + k0);
+      const float sx = w_pow2(15 - e - 2 * p);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hv[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        hv[2 * j] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(w[j] & 0xffffu) * sx));
+        hv[2 * j + 1] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(w[j] >> 16) * sx));
+      }
+      out.x = hv[0] | (hv[2] << 16);
+      out.y = hv[1] | (hv[3] << 16);
+      out.z = hv[4] | (hv[6] << 16);
+      out.w = hv[5] | (hv[7] << 16);
+    }
+    *reinterpret_cast<uint4*>(bbuf + (static_cast<int64_t>(it) * ncol + m) * 16) = out;
+  }
+  // group sums XS[m][g] (fixed order: lanes, then a butterfly)
+  for (int gi = warp; gi < KG; gi += kWPrepThreads / 32) {
+    float s = 0.0f;
+    if (live)
+      for (int i = lane; i < G; i += 32) s += bf16_bits_to_float(xr[gi * G + i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) xs[m * KG + gi] = s;
+  }
+}
+
+// ---- the pass: NCOL = MMA N (16 .. 80), the pass's hidden rows in columns 0 .. R-1 -------------
+template <int G, int NCOL>
+__global__ void __launch_bounds__(kWThreads, 1)
+    coarse_wide_kernel(const __grid_constant__ CUtensorMap tmap, const WideArgs a) {
+  constexpr int P = 4;           // int2 planes
+  constexpr int CPJ = G / 16;    // chunks per scale group
+  constexpr int ACOLS = 8 * P;   // TMEM columns of one A stage
+  constexpr int NA = (kWTmemCols - 2 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
+                                                                : (kWTmemCols - 2 * NCOL) / ACOLS;
+  constexpr int PITCH = NCOL + 1;  // words per row of the key buffer (odd: no bank conflicts)
+  static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 80, "MMA N");
+  static_assert(NA >= 4, "TMEM budget");
+  extern __shared__ unsigned char sm_raw[];
+  // 1024-byte alignment for the 128-byte swizzle of the packed ring
+  unsigned char* sm = sm_raw + ((1024u - (smem_addr(sm_raw) & 1023u)) & 1023u);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int np = a.np, nbu = a.nbu;
+  uint64_t* pfull = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kWMaxNP] stage landed
+  uint64_t* pempty = pfull + kWMaxNP;   // [kWMaxNP] stage read by the dequantising warps
+  uint64_t* bfull = pempty + kWMaxNP;   // [kWMaxNB] B unit landed
+  uint64_t* bempty = bfull + kWMaxNB;   // [kWMaxNB] B unit's MMAs done
+  uint64_t* afull = bempty + kWMaxNB;   // [kWMaxNA] A stage written
+  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA] A stage's MMAs done
+  uint64_t* dfull = aempty + kWMaxNA;   // [2] D slot complete
+  uint64_t* dempty = dfull + 2;         // [2] D slot read by the fold warps
+  uint64_t* mma_done = dempty + 2;      // every MMA of the CTA complete
+  uint64_t* keys_ready = mma_done + 1;  // a tile's keys written by the fold warps
+  uint64_t* keys_free = mma_done + 2;   // ... and consumed by the selection warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int my_tiles =
+      (a.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+      static_cast<int>(gridDim.x);
+  const int total_stages = my_tiles * a.NS;
+  const int units_per_tile = a.NJ * P;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWMaxNP; ++i) {
+      mbar_init(&pfull[i], 1u);
+      mbar_init(&pempty[i], 4u);
+    }
+    for (int i = 0; i < kWMaxNB; ++i) {
+      mbar_init(&bfull[i], 1u);
+      mbar_init(&bempty[i], 1u);
+    }
+    for (int i = 0; i < kWMaxNA; ++i) {
+      mbar_init(&afull[i], 4u);
+      mbar_init(&aempty[i], 1u);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&dfull[i], 1u);
+      mbar_init(&dempty[i], 8u);  // the 8 fold warps
+    }
+    mbar_init(mma_done, 1u);
+    mbar_init(keys_ready, 8u);
+    mbar_init(keys_free, 4u);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_map(&tmap);
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kWTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t a_base = tmem + 2 * NCOL;  // column of A stage 0 (D slots at 0 and NCOL)
+
+  // Bounded wait on one phase of an mbarrier. Returns at once (false) once the launch is
+  // aborted; a wait that runs out aborts it. Callers go on either way (uniform control flow).
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      if (*abort_flag) return false;
+      if (mbar_try_wait(bar, parity)) return true;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        set_status(a.status, DH_DEV_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  };
+  auto tile_of = [&](int lt) {
+    return static_cast<int>(blockIdx.x) + lt * static_cast<int>(gridDim.x);
+  };
+
+  int issued = 0, issued_b = 0;  // copies issued by warp 0 / warp 2 (lane 0)
+  if (warp == 0) {
+    // ---- packed rows: ring stages in order (weights: no wait on the preceding kernel) ---------
+    if (lane == 0) {
+      for (; issued < total_stages; ++issued) {
+        const int slot = issued % np;
+        if (issued >= np) wait_bar(&pempty[slot], static_cast<uint32_t>(issued / np - 1) & 1u);
+        if (*abort_flag) break;
+        const int lt = issued / a.NS, s = issued - lt * a.NS;
+        mbar_arrive_expect_tx(&pfull[slot], static_cast<uint32_t>(kWStageSmem));
+        tma_load_2d(sm + slot * kWStageSmem, &tmap, s * kWStageBytes, tile_of(lt) * kWRows,
+                    &pfull[slot]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---- B units (the prep kernel's output): one per (tile, group, plane), in MMA order --------
+    if (lane == 0) {
+      grid_dependency_wait();
+      const int total_units = my_tiles * units_per_tile;
+      for (; issued_b < total_units; ++issued_b) {
+        const int slot = issued_b % nbu;
+        if (issued_b >= nbu)
+          wait_bar(&bempty[slot], static_cast<uint32_t>(issued_b / nbu - 1) & 1u);
+        if (*abort_flag) break;
+        const int unit = issued_b % units_per_tile;
+        mbar_arrive_expect_tx(&bfull[slot], static_cast<uint32_t>(a.unit_bytes));
+        bulk_g2s(sm + a.off_bring + slot * a.unit_bytes,
+                 a.bbuf + static_cast<int64_t>(unit) * a.unit_bytes,
+                 static_cast<uint32_t>(a.unit_bytes), &bfull[slot]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issue: per (group J, plane p) the group's chunks into one D slot -----------------
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc_f16(kWRows, NCOL);
+      const uint32_t b_ring = smem_addr(sm + a.off_bring);
+      int gslot = 0, gu = 0;
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        for (int J = 0; J < a.NJ; ++J) {
+          for (int p = 0; p < P; ++p, ++gslot, ++gu) {
+            const int bslot = gu % nbu, dbuf = gslot & 1;
+            wait_bar(&bfull[bslot], static_cast<uint32_t>(gu / nbu) & 1u);
+            if (gslot >= 2) wait_bar(&dempty[dbuf], static_cast<uint32_t>((gslot >> 1) - 1) & 1u);
+            tc_fence_after();
+            const uint32_t unit = b_ring + bslot * a.unit_bytes;
+            for (int cj = 0; cj < CPJ; ++cj) {
+              const int ga = lt * a.NC + J * CPJ + cj, aslot = ga % NA;
+              if (p == 0) {
+                wait_bar(&afull[aslot], static_cast<uint32_t>(ga / NA) & 1u);
+                tc_fence_after();
+              }
+              const uint64_t bdesc = tc_sdesc(unit + cj * (2 * NCOL * 16), NCOL * 16, 128u);
+              tc_mma_f16_ts(tmem + dbuf * NCOL, a_base + aslot * ACOLS + 8 * p, bdesc, idesc,
+                            cj != 0);
+              if (p == P - 1) tc_commit(&aempty[aslot]);
+            }
+            tc_commit(&bempty[bslot]);
+            tc_commit(&dfull[dbuf]);
+          }
+        }
+      }
+      tc_commit(mma_done);
+      mbar_wait_bounded(mma_done, 0u);  // also after an abort: no MMA may outlive the TMEM
+    }
+    __syncwarp();
+  } else if (warp < 7) {
+    // ---- dequantisation: every chunk of every tile, one thread per row --------------------------
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t my_a = a_base + tmem_lane_base(warp);
+    const int sw = row & 7;
+    int gs_cur = -1;
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      for (int c = 0; c < a.NC; ++c) {
+        const int ga = lt * a.NC + c, gs = lt * a.NS + (c >> 3);
+        if (gs != gs_cur) {
+          if (gs_cur >= 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[gs_cur % np]);
+          }
+          wait_bar(&pfull[gs % np], static_cast<uint32_t>(gs / np) & 1u);
+          __syncwarp();
+          gs_cur = gs;
+        }
+        const int slot = ga % NA;
+        if (ga >= NA) {
+          wait_bar(&aempty[slot], static_cast<uint32_t>(ga / NA - 1) & 1u);
+          __syncwarp();
+        }
+        tc_fence_after();
+        const uint4 w4 = *reinterpret_cast<const uint4*>(
+            sm + (gs % np) * kWStageSmem + row * kWStageBytes + (((c & 7) ^ sw) << 4));
+        const uint32_t t[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t r[32];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t te = t[w], to = t[w] >> 8;
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            r[8 * p + 2 * w] = te & (0x00030003u << (2 * p));
+            r[8 * p + 2 * w + 1] = to & (0x00030003u << (2 * p));
+          }
+        }
+        tmem_st_x32(my_a + slot * ACOLS, r);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[slot]);
+      }
+    }
+    if (gs_cur >= 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pempty[gs_cur % np]);
+    }
+  } else {
+    // ---- fold: two warps per TMEM lane quadrant, each NCOL/2 columns of its 32 rows ----------------
+    if (warp < 15) {
+      constexpr int HC = NCOL / 2;  // columns of this warp
+      const int fw = warp - 7;      // 0..7
+      const int half = fw >> 2;
+      const int row = (warp & 3) * 32 + lane;
+      const int col0 = half * HC;
+      const uint32_t my_d = tmem + tmem_lane_base(warp) + col0;
+      unsigned char* s_row = sm + a.off_sz + row * a.szp;  // this row's S ...
+      unsigned char* z_row = s_row + kWRows * a.szp;       // ... and ZS
+      uint32_t* keys = reinterpret_cast<uint32_t*>(sm + a.off_keys);  // [128][PITCH]
+      float* xsd = reinterpret_cast<float*>(sm + a.off_xs);           // [KG][NCOL]
+      int* ew_s = reinterpret_cast<int*>(sm + a.off_ew);              // [NCOL]
+      // the half-0 warp copies the row's S, the half-1 warp its ZS (weights' scales: no wait on
+      // the preceding kernel); a barrier of the fold warps then shares them
+      auto load_sz = [&](int lt) {
+        const int n = tile_of(lt) * kWRows + row;
+        const bool valid = n < a.N;
+        const int64_t off = static_cast<int64_t>(valid ? n : 0) * a.KG;
+        const uint16_t* src = (half ? a.ZS : a.S) + off;
+        unsigned char* dst = half ? z_row : s_row;
+        for (int i = 0; i < a.KG / 8; ++i) w_cp_async16(smem_addr(dst + 16 * i), src + 8 * i, valid);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      };
+      if (my_tiles > 0) load_sz(0);
+      // the prep kernel's group sums and exponents (the outputs are written after this wait
+      // too): XS in the units of the D slots, 2^24 / (2^(15 - E_m) 4) = 2^(E_m + 7), as
+      // xsd[g][m] = XS[m][g] 2^-(E_m + 7) (a power of two: exact)
+      grid_dependency_wait();
+      const int ftid = fw * 32 + lane;
+      if (ftid < NCOL) ew_s[ftid] = a.ew[ftid];
+      for (int i = ftid; i < NCOL * a.KG; i += 256) {
+        const int m = i / a.KG, gi = i - m * a.KG;
+        xsd[gi * NCOL + m] = a.xs[i] * w_pow2(-(a.ew[m] + 7));
+      }
+      named_bar_sync(2, 256);
+      int gslot = 0;
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        const int n = tile_of(lt) * kWRows + row;
+        const bool valid = n < a.N;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        named_bar_sync(2, 256);  // both halves' copies of the tile's S and ZS rows have landed
+        float acc[HC];
+#pragma unroll
+        for (int m = 0; m < HC; ++m) acc[m] = 0.0f;
+        // the tile's D slots, in the order the MMAs complete them: (group J, plane p); each adds
+        // S_g D_g and the zero-point part (S_g - ZS_g) XS_g
+        for (int J = 0; J < a.NJ; ++J) {
+          for (int p = 0; p < P; ++p, ++gslot) {
+            const int dbuf = gslot & 1, gi = p * a.NJ + J;
+            wait_bar(&dfull[dbuf], static_cast<uint32_t>(gslot >> 1) & 1u);
+            __syncwarp();
+            tc_fence_after();
+            const float sg = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(s_row + 2 * gi));
+            const float zg = sg - bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(z_row + 2 * gi));
+            const float* xg = xsd + gi * NCOL + col0;
+#pragma unroll
+            for (int q = 0; q < HC; q += 8) {
+              uint32_t d[8];
+              tmem_ld<8>(my_d + dbuf * NCOL + q, d);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[q + i] = fmaf(sg, __uint_as_float(d[i]), fmaf(zg, xg[q + i], acc[q + i]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[dbuf]);
+          }
+        }
+        named_bar_sync(2, 256);  // both halves are done with the tile's S and ZS rows
+        if (lt + 1 < my_tiles) load_sz(lt + 1);
+#pragma unroll
+        for (int m = 0; m < HC; ++m) acc[m] *= w_pow2(ew_s[col0 + m] + 7);  // logit units
+        if (a.y != nullptr && valid) {
+#pragma unroll
+          for (int m = 0; m < HC; ++m)
+            if (col0 + m < a.R)
+              a.y[static_cast<int64_t>(a.m0 + col0 + m) * a.N + n] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+        }
+        // hand the keys to the selection warps (a single buffer: wait until they are done with
+        // the previous tile's)
+        if (lt > 0) wait_bar(keys_free, static_cast<uint32_t>(lt - 1) & 1u);
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < HC; ++m)
+          keys[row * PITCH + col0 + m] = valid ? order_key(acc[m]) : 0u;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(keys_ready);
+      }
+    } else {
+      // ---- selection: block top-KCAND of every (64-row block, hidden row) of a tile -----------
+      grid_dependency_wait();  // the outputs
+      const int sw4 = warp - 15;  // 0..3
+      const uint32_t* keys = reinterpret_cast<const uint32_t*>(sm + a.off_keys);
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        const int tile = tile_of(lt);
+        wait_bar(keys_ready, static_cast<uint32_t>(lt) & 1u);
+        __syncwarp();
+        // job j = (64-row block j / R of the tile, hidden row j % R)
+        for (int j = sw4; j < 2 * a.R; j += 4) {
+          const int blk = j / a.R, m = j - blk * a.R;
+          const int b = tile * 2 + blk;
+          if (b >= a.nblk) continue;
+          const uint32_t* kc = keys + 64 * blk * PITCH + m;
+          uint32_t k0 = kc[lane * PITCH], k1 = kc[(lane + 32) * PITCH];
+          uint32_t key_lo = 0u, row_lo = 64u, key_hi = 0u, row_hi = 64u;  // slots lane, lane + 32
+          for (int r = 0; r < a.kcand; ++r) {
+            const bool first = k0 >= k1;
+            const uint32_t bk = first ? k0 : k1;
+            const uint32_t brow =
+                first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t rwin = __reduce_min_sync(0xffffffffu, bk == kmax ? brow : 64u);
+            if (kmax != 0u && lane == static_cast<int>(rwin & 31u)) {
+              if (rwin < 32u) k0 = 0u; else k1 = 0u;
+            }
+            if (lane == (r & 31)) {
+              if (r < 32) {
+                key_lo = kmax;
+                row_lo = kmax ? rwin : 64u;
+              } else {
+                key_hi = kmax;
+                row_hi = kmax ? rwin : 64u;
+              }
+            }
+          }
+          const int64_t obase = static_cast<int64_t>(a.m0 + m) * a.nblk * a.kcand +
+                                static_cast<int64_t>(b) * a.kcand;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int slot = lane + 32 * h;
+            const uint32_t kk = h ? key_hi : key_lo, rr = h ? row_hi : row_lo;
+            if (slot < a.kcand) {
+              a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
+              a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(keys_free);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 0 || warp == 2) {
+    // after an abort, copies may still be in flight: they land before the CTA's shared memory
+    // goes away
+    if (lane == 0 && *abort_flag) {
+      const int n_iss = warp == 0 ? issued : issued_b, depth = warp == 0 ? np : nbu;
+      uint64_t* bars = warp == 0 ? pfull : bfull;
+      for (int s = 0; s < depth && s < n_iss; ++s) {
+        const int last = n_iss - 1 - ((n_iss - 1 - s) % depth);
+        mbar_wait_bounded(&bars[s], static_cast<uint32_t>(last / depth) & 1u);
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kWTmemCols);
+  }
+}
+
+// ---- host side ----------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+static size_t round_up_sz(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+size_t coarse_wide_scratch_bytes(int64_t M, int64_t K) {
+  if (M <= kWideMinRows) return 0;
+  const size_t kk = static_cast<size_t>(K);
+  return round_up_sz(kWideMaxRows * kk * 2, 256) +          // B units
+         round_up_sz(kWideMaxRows * (kk / 64) * 4, 256) +   // group sums (G >= 64)
+         round_up_sz(kWideMaxRows * 4, 256);                // exponents
+}
+
+bool coarse_wide_supports(const CoarseCall& cc) {
+  if (cc.bits != 2 || (cc.G != 64 && cc.G != 128) || cc.M <= kWideMinRows) return false;
+  if (cc.K % 512 != 0 || (cc.K / cc.G) % 8 != 0 || cc.K > 65536) return false;
+  return encode_tiled_fn() != nullptr;
+}
+
+// Shared-memory plan of a pass; false if the rings do not fit.
+static bool plan_wide(WideArgs& a, int ncol, int G, int max_smem, int* smem_bytes) {
+  const int cpj = G / 16;
+  a.unit_bytes = cpj * 2 * ncol * 16;
+  a.szp = a.KG * 2;
+  const int sz_bytes = 2 * kWRows * a.szp;
+  const int key_bytes = kWRows * (ncol + 1) * 4;
+  const int xs_bytes = ncol * a.KG * 4;
+  const int ew_bytes = ncol * 4;
+  const int bar_bytes = (2 * kWMaxNP + 2 * kWMaxNB + 2 * kWMaxNA + 4 + 3) * 8 + 16;
+  const int fixed = sz_bytes + key_bytes + xs_bytes + ew_bytes + bar_bytes + 64 + 1024;
+  int nbu = kWMaxNB, np = 0;
+  for (; nbu >= 2; --nbu) {
+    np = (max_smem - fixed - nbu * a.unit_bytes) / kWStageSmem;
+    if (np >= 3) break;
+  }
+  if (np > kWMaxNP) np = kWMaxNP;
+  if (nbu < 2 || np < 3) return false;
+  a.np = np;
+  a.nbu = nbu;
+  a.off_bring = np * kWStageSmem;
+  a.off_sz = a.off_bring + nbu * a.unit_bytes;
+  a.off_keys = a.off_sz + sz_bytes;
+  a.off_xs = a.off_keys + key_bytes;
+  a.off_ew = a.off_xs + xs_bytes;
+  a.off_bars = static_cast<int>(round_up_sz(a.off_ew + ew_bytes, 16));
+  *smem_bytes = a.off_bars + bar_bytes + 1024;
+  return *smem_bytes <= max_smem;
+}
+
+template <typename Kernel, typename... Args>
+static cudaError_t launch_pdl(Kernel kernel, int grid, int threads, int smem, cudaStream_t s,
+                              Args... args) {
+  // programmatic dependent launch: the CTAs may start while the kernel before them in the
+  // stream finishes; they wait for it (griddepcontrol.wait) before touching its outputs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int G, int NCOL>
+static cudaError_t launch_wide_pass(const CUtensorMap& map, const WideArgs& a, int grid, int smem,
+                                    const uint16_t* x, unsigned char* bbuf, float* xs, int* ew,
+                                    cudaStream_t s) {
+  cudaError_t e = launch_pdl(wide_prep_kernel<G>, NCOL, kWPrepThreads, 0, s, x, a.m0, a.R, a.K,
+                             NCOL, bbuf, xs, ew);
+  if (e != cudaSuccess) return e;
+  auto kernel = coarse_wide_kernel<G, NCOL>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kernel, grid, kWThreads, smem, s, map, a);
+}
+
+template <int G>
+static cudaError_t launch_wide_g(int ncol, const CUtensorMap& map, const WideArgs& a, int grid,
+                                 int smem, const uint16_t* x, unsigned char* bbuf, float* xs,
+                                 int* ew, cudaStream_t s) {
+  switch (ncol) {
+    case 32: return launch_wide_pass<G, 32>(map, a, grid, smem, x, bbuf, xs, ew, s);
+    case 48: return launch_wide_pass<G, 48>(map, a, grid, smem, x, bbuf, xs, ew, s);
+    case 64: return launch_wide_pass<G, 64>(map, a, grid, smem, x, bbuf, xs, ew, s);
+    default: return launch_wide_pass<G, 80>(map, a, grid, smem, x, bbuf, xs, ew, s);
+  }
+}
+
+cudaError_t launch_coarse_wide(const CoarseCall& cc, void* scratch, int num_sms, int max_smem,
+                               cudaStream_t s) {
+  if (!coarse_wide_supports(cc) || scratch == nullptr) return cudaErrorNotSupported;
+  WideArgs a{};
+  a.K = static_cast<int>(cc.K);
+  a.N = static_cast<int>(cc.N);
+  a.RB = a.K / 4;
+  a.KG = a.K / cc.G;
+  a.NJ = a.RB / cc.G;
+  a.NC = a.RB / 16;
+  a.NS = a.RB / kWStageBytes;
+  a.ntiles = (a.N + kWRows - 1) / kWRows;
+  a.S = static_cast<const uint16_t*>(cc.S);
+  a.ZS = static_cast<const uint16_t*>(cc.ZS);
+  a.kcand = cc.kcand;
+  a.nblk = static_cast<int>((cc.N + 63) / 64);
+  a.cand_val = cc.cand_val;
+  a.cand_id = cc.cand_id;
+  a.y = static_cast<uint16_t*>(cc.y);
+  a.status = cc.status;
+  const size_t kk = static_cast<size_t>(cc.K);
+  unsigned char* bbuf = static_cast<unsigned char*>(scratch);
+  float* xs = reinterpret_cast<float*>(bbuf + round_up_sz(kWideMaxRows * kk * 2, 256));
+  int* ew = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(xs) +
+                                   round_up_sz(kWideMaxRows * (kk / 64) * 4, 256));
+  a.bbuf = bbuf;
+  a.xs = xs;
+  a.ew = ew;
+
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.RB), static_cast<cuuint64_t>(a.N)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.RB)};
+  const cuuint32_t box[2] = {kWStageBytes, kWRows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode_tiled_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cc.packed),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  const int grid = a.ntiles < num_sms ? a.ntiles : num_sms;
+  const int64_t passes = (cc.M + kWideMaxRows - 1) / kWideMaxRows;
+  for (int64_t ps = 0; ps < passes; ++ps) {
+    // rows spread evenly over the passes, each a multiple of 16 columns wide
+    const int64_t m0 = ps * cc.M / passes, m1 = (ps + 1) * cc.M / passes;
+    a.m0 = static_cast<int>(m0);
+    a.R = static_cast<int>(m1 - m0);
+    const int ncol = a.R <= 32 ? 32 : a.R <= 48 ? 48 : a.R <= 64 ? 64 : 80;
+    int smem = 0;
+    if (!plan_wide(a, ncol, cc.G, max_smem, &smem)) return cudaErrorInvalidValue;
+    const cudaError_t e =
+        cc.G == 128
+            ? launch_wide_g<128>(ncol, map, a, grid, smem, static_cast<const uint16_t*>(cc.x),
+                                 bbuf, xs, ew, s)
+            : launch_wide_g<64>(ncol, map, a, grid, smem, static_cast<const uint16_t*>(cc.x),
+                                bbuf, xs, ew, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace dh

@@ -19,6 +19,7 @@ struct CoarseCall {
   int32_t* cand_id;
   void* y;
   uint32_t* status;
+  void* scratch;  // the coarse pass's part of the workspace (coarse_wide_scratch_bytes)
 };
 
 struct RerankCall {
@@ -41,8 +42,19 @@ cudaError_t launch_quantize_pack(int bits, const void* W, int64_t N, int64_t K, 
                                  uint8_t* packed, void* S, void* ZS, cudaStream_t s);
 // cudaErrorInvalidValue: the shape does not fit the kernel's shared-memory plan.
 cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s);
+// The tensor-core (tcgen05) pass of int2 heads for more than kWideMinRows hidden rows, up to
+// kWideMaxRows per pass (coarse_tc.cu). Its scratch (the hidden states laid out as the MMA
+// operand, their group sums and scales) lives in the caller's workspace.
+constexpr int kWideMinRows = 16;
+constexpr int kWideMaxRows = 80;
+size_t coarse_wide_scratch_bytes(int64_t M, int64_t K);
+bool coarse_wide_supports(const CoarseCall& cc);
+cudaError_t launch_coarse_wide(const CoarseCall& cc, void* scratch, int num_sms, int max_smem,
+                               cudaStream_t s);
 cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s);
 // Sets the calling thread's dh_last_error() message; returns `code`.
 int record_error(int code, const char* msg);
+// Workspace bytes dh_draft_head_rerank_argmax requires (independent of the sizes).
+size_t rerank_workspace_needed();
 
 }  // namespace dh

@@ -56,7 +56,7 @@ extern "C" int dh_draft_head_rerank_argmax_noalloc(const void* x, int64_t M, int
                                                    int rerank, int32_t* rr_id, float* rr_logit,
                                                    int32_t* argmax_id, void* y_coarse,
                                                    dh_stream_t s) {
-  const size_t need = dh_workspace_bytes(M, N, K, 1, rerank);
+  const size_t need = M < 1 ? 0 : dh::rerank_workspace_needed();
   if (need == 0) {
     char msg[160];
     snprintf(msg, sizeof msg, "draft_head_rerank_argmax_noalloc: M=%lld out of range",

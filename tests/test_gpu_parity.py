@@ -70,6 +70,12 @@ COARSE_CASES = [
     (3, 2048, 58400, 64, 2, 4, 19),
     (4, 5120, 124160, 128, 2, 8, 20),
     (6, 2048, 30000, 128, 4, 2, 21),
+    # more than 16 hidden rows of an int2 head: the tensor-core pass (tcgen05)
+    (17, 1024, 8232, 128, 2, 8, 22),    # ragged N, 32 MMA columns, 17 rows
+    (72, 2048, 4100, 64, 2, 8, 23),     # G = 64, 80 columns
+    (40, 5120, 20000, 128, 2, 3, 24),   # K = 5120, 48 columns, odd KCAND
+    (97, 1024, 3000, 128, 2, 8, 25),    # two passes (48 + 49 rows)
+    (72, 5120, 124160, 128, 2, 8, 26),  # the vocabulary-scale head at 72 rows
 ]
 
 
@@ -160,6 +166,7 @@ E2E_CASES = [
     (13, 1024, 3000, 128, 2, 5, 16, 12),
     (5, 1024, 2048, 128, 4, 1, 16, 13),
     (4, 5120, 8192, 128, 2, 8, 32, 17),
+    (72, 5120, 20000, 128, 2, 8, 16, 27),  # tensor-core coarse pass, then the rerank
 ]
 
 
