@@ -161,11 +161,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
   constexpr int P = 4;           // int2 planes
   constexpr int CPJ = G / 16;    // chunks per scale group
   constexpr int ACOLS = 8 * P;   // TMEM columns of one A stage
-  constexpr int NA = (kWTmemCols - 2 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
-                                                                : (kWTmemCols - 2 * NCOL) / ACOLS;
+  // A stages, an even number: they are released in pairs (chunks 2q, 2q + 1), one commit each
+  constexpr int NA = ((kWTmemCols - 2 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
+                                                                  : (kWTmemCols - 2 * NCOL) / ACOLS) &
+                     ~1;
   constexpr int PITCH = NCOL + 1;  // words per row of the key buffer (odd: no bank conflicts)
   static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 80, "MMA N");
-  static_assert(NA >= 4, "TMEM budget");
+  static_assert(NA >= CPJ + 2, "TMEM budget: a group's chunks plus one spare pair");
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte alignment for the 128-byte swizzle of the packed ring
   unsigned char* sm = sm_raw + ((1024u - (smem_addr(sm_raw) & 1023u)) & 1023u);
@@ -175,9 +177,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
   uint64_t* pfull = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kWMaxNP] stage landed
   uint64_t* pempty = pfull + kWMaxNP;   // [kWMaxNP] stage read by the dequantising warps
   uint64_t* bfull = pempty + kWMaxNP;   // [kWMaxNB] B unit landed
-  uint64_t* bempty = bfull + kWMaxNB;   // [kWMaxNB] B unit's MMAs done
+  uint64_t* bempty = bfull + kWMaxNB;   // [kWMaxNB] B unit's D slot read (its MMAs are done)
   uint64_t* afull = bempty + kWMaxNB;   // [kWMaxNA] A stage written
-  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA] A stage's MMAs done
+  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA / 2] A stage pair's MMAs done
   uint64_t* dfull = aempty + kWMaxNA;   // [2] D slot complete
   uint64_t* dempty = dfull + 2;         // [2] D slot read by the fold warps
   uint64_t* mma_done = dempty + 2;      // every MMA of the CTA complete
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
     for (int i = 0; i < kWMaxNB; ++i) {
       mbar_init(&bfull[i], 1u);
-      mbar_init(&bempty[i], 1u);
+      mbar_init(&bempty[i], 8u);  // the 8 fold warps
     }
     for (int i = 0; i < kWMaxNA; ++i) {
       mbar_init(&afull[i], 4u);
@@ -298,9 +300,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
               const uint64_t bdesc = tc_sdesc(unit + cj * (2 * NCOL * 16), NCOL * 16, 128u);
               tc_mma_f16_ts(tmem + dbuf * NCOL, a_base + aslot * ACOLS + 8 * p, bdesc, idesc,
                             cj != 0);
-              if (p == P - 1) tc_commit(&aempty[aslot]);
+              if (p == P - 1 && (cj & 1)) tc_commit(&aempty[aslot >> 1]);
             }
-            tc_commit(&bempty[bslot]);
+            // one commit per unit: the fold warps that read the D slot also release the B unit
             tc_commit(&dfull[dbuf]);
           }
         }
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
         const int slot = ga % NA;
         if (ga >= NA) {
-          wait_bar(&aempty[slot], static_cast<uint32_t>(ga / NA - 1) & 1u);
+          wait_bar(&aempty[slot >> 1], static_cast<uint32_t>(ga / NA - 1) & 1u);
           __syncwarp();
         }
         tc_fence_after();
@@ -425,7 +427,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&dempty[dbuf]);
+            if (lane == 0) {
+              mbar_arrive(&dempty[dbuf]);
+              mbar_arrive(&bempty[gslot % nbu]);  // the slot's MMAs, and so its B unit, are done
+            }
           }
         }
         named_bar_sync(2, 256);  // both halves are done with the tile's S and ZS rows
