@@ -82,7 +82,10 @@ size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits);
 
 /* Workspace bytes the two per-call entry points need for these sizes (one workspace serves
  * both). The workspace must be zero-filled once before first use; calls sharing a workspace
- * must be ordered on one stream. */
+ * must be ordered on one stream. The rerank needs the 256-byte header (status word) only; the
+ * coarse pass of more than 16 hidden rows of an int2 head (its tensor-core path) also keeps its
+ * scratch after the header: the hidden states laid out as the MMA operand (80 * K * 2 bytes),
+ * their group sums and scales. */
 size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank);
 
 /*
@@ -98,7 +101,13 @@ size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank
  *             slots past the block's last valid row hold (-inf, -1).
  *   cand_id   i32 [M, nblk*kcand] out: the vocab row of each slot.
  *   y_coarse  bf16 [M, N] out or NULL: bf16(c), the coarse logits.
- *   workspace device buffer of ws_bytes >= dh_workspace_bytes(...), 256-B aligned.
+ *   workspace device buffer of ws_bytes >= dh_workspace_bytes(M, N, K, ...), 256-B aligned.
+ * Up to 16 hidden rows (and every int4 call) run on warp-level MMAs in passes of 8 rows; more
+ * than 16 rows of an int2 head run on the 5th-generation tensor cores in passes of up to 80.
+ * The kernels are launched as programmatic dependents: they read the weights (packed, S, ZS)
+ * before the preceding kernel in the stream has completed if that kernel lets its dependents
+ * start early (this library's rerank does), and x and every output only after it. So the
+ * weights must not be written by such a kernel directly before this call.
  */
 int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
                               const void* S, const void* ZS, int64_t N, int G, int bits,
