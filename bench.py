@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--extra-m", default="8,72", help="supplementary row counts ('' = none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the int4 / group-64 comparison lines (M=8)")
     p.add_argument("--no-soak", action="store_true",
                    help="skip the 1.5 s clock-sampling soak (profiling runs)")
     p.add_argument("--copies", type=int, default=COPIES,
@@ -163,12 +165,12 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     nblk = (N_VOCAB + 63) // 64
 
-    def measure(M, steps, warmup, record_launches):
+    def measure(M, steps, warmup, record_launches, bits=2, group=GROUP, kcand=KCAND, packs=packs):
         xs = [torch.from_numpy(xs_h[c, :M].copy().view(np.int16)).to(dev).view(torch.bfloat16)
               for c in range(ncopy)]
-        ws = dh.new_workspace(M, N_VOCAB, K_DIM, KCAND, RERANK, dev)
-        cv = torch.empty(M, nblk * KCAND, dtype=torch.float32, device=dev)
-        ci = torch.empty(M, nblk * KCAND, dtype=torch.int32, device=dev)
+        ws = dh.new_workspace(M, N_VOCAB, K_DIM, kcand, RERANK, dev)
+        cv = torch.empty(M, nblk * kcand, dtype=torch.float32, device=dev)
+        ci = torch.empty(M, nblk * kcand, dtype=torch.int32, device=dev)
         rr = torch.empty(M, RERANK, dtype=torch.int32, device=dev)
         rl = torch.empty(M, RERANK, dtype=torch.float32, device=dev)
         am = torch.empty(M, dtype=torch.int32, device=dev)
@@ -176,8 +178,8 @@ def run_ours(args, rank, world):
 
         def step(c, coarse_only=False):
             p, S, ZS = packs[c]
-            dh.dh_draft_head_coarse_topk(xs[c], p, S, ZS, N_VOCAB, GROUP, 2, KCAND, cand_val=cv,
-                                         cand_id=ci, workspace=ws)
+            dh.dh_draft_head_coarse_topk(xs[c], p, S, ZS, N_VOCAB, group, bits, kcand,
+                                         cand_val=cv, cand_id=ci, workspace=ws)
             if not coarse_only:
                 dh.dh_draft_head_rerank_argmax(xs[c], Ws[c], cv, ci, RERANK, rr_id=rr,
                                                rr_logit=rl, argmax_id=am, workspace=ws)
@@ -249,7 +251,11 @@ def run_ours(args, rank, world):
     peak, peak_kind = measured_peaks()
     alg_coarse = dh.dh_packed_bytes(N_VOCAB, K_DIM, GROUP, 2)
     alg_call = alg_coarse + args.m * RERANK * K_DIM * 2
-    launches_per_step = (args.m + 7) // 8 + 1
+    def launches_per_call(M):
+        # coarse: passes of 8 rows up to 16 rows; beyond, a prep and a tensor-core kernel per
+        # pass of up to 80 rows; then the rerank
+        return ((M + 7) // 8 if M <= 16 else 2 * ((M + 79) // 80)) + 1
+    launches_per_step = launches_per_call(args.m)
 
     extra = {}
     for M in extra_ms(args):
@@ -260,6 +266,23 @@ def run_ours(args, rank, world):
                          "coarse_us": round(1e3 * cm / steps, 3),
                          "hbm_gbs_per_call": round((alg_coarse + M * RERANK * K_DIM * 2) / u / 1e3, 1),
                          "steps": steps}
+    # the page's two ablations at M=8 (the comparison workload): the 4-bit head with KCAND=1, and
+    # the int2 head with 64-wide groups
+    variants = {}
+    if not args.no_variants:
+        for name, bits, group, kc, per in (("int4_g128_m8_kcand1", 4, 128, 1, 2),
+                                           ("int2_g64_m8_kcand8", 2, 64, KCAND, 4)):
+            quant = dh.dh_quantize_pack_int4 if bits == 4 else dh.dh_quantize_pack_int2
+            vp = [quant(Wc, group) for Wc in Ws]
+            steps = max(50, min(args.steps, 1000))
+            mm, cm = measure(8, steps, 8, True, bits=bits, group=group, kcand=kc, packs=vp)
+            u = mm * 1e3 / steps
+            alg = dh.dh_packed_bytes(N_VOCAB, K_DIM, group, bits) + 8 * RERANK * K_DIM * 2
+            variants[name] = {"us_per_call": round(u, 3), "coarse_us": round(1e3 * cm / steps, 3),
+                              "algorithmic_bytes_per_call": alg,
+                              "hbm_gbs_per_call": round(alg / u / 1e3, 1), "steps": steps}
+            del vp
+            torch.cuda.synchronize()
 
     e2e = None
     if not args.no_e2e:
@@ -287,7 +310,8 @@ def run_ours(args, rank, world):
                          f"({ncopy * alg_coarse / 1e6:.0f} MB) and of the bf16 head",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs_per_call": round(alg_call / us_step / 1e3, 1),
-        "roofline": {"bound": "hbm", "kernel": "coarse_topk_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": "coarse_topk_kernel" if args.m <= 16 else "coarse_wide_kernel",
                      "achieved": round(alg_coarse / coarse_us / 1e3, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(alg_coarse / coarse_us / 1e3 / peak, 4),
                      "peak_kind": peak_kind,
@@ -297,6 +321,7 @@ def run_ours(args, rank, world):
         "gpu_launches": args.steps * launches_per_step,
         "clocks": dict(clk, window=f"timed region + {soak_t:.1f} s of the same step"),
         "per_m": extra,
+        "variants": variants,
     }
     if e2e is not None:
         line["e2e"] = e2e

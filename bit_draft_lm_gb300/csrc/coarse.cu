@@ -21,29 +21,33 @@ static int plan_coarse(CoarseArgs& a, int max_smem, int nsw_max) {
   a.NW = a.K / 256;
   const int mt_max = a.M < 8 ? a.M : 8;
   a.red_pitch = mt_max | 1;  // odd: a warp reading one column over 32 rows hits 32 banks
-  int off = 0;
-  a.off_bars = off;
-  off += (kSBlocks + kMaxRedBufs) * 8 + (3 * kMaxRedBufs + kSBlocks + 2) * 4 + 16;
-  a.off_xs = off = (off + 15) / 16 * 16;
-  off += a.NW * 8 * 4 * 4;  // strip group sums: [NW][8 rows][<= 4 groups] fp32
-  off += mt_max * a.KG * 4;  // group sums of the row: [mt][K/G] fp32
-  a.off_zb = off = (off + 15) / 16 * 16;
-  off += (a.KG / 8) * 3 * mt_max * 4 * 8;  // zero-point MMA B fragments: [K/G/8][3][mt][4] uint2
-  a.off_sz = off = (off + 127) / 128 * 128;
-  off += kSBlocks * 2 * kBlockRows * a.KG * 2;
-  a.off_red = off = (off + 15) / 16 * 16;
   const int red_buf = (a.NW + 1) * kBlockRows * a.red_pitch * 4;  // NW warps + zero-point slot
   const int wstage = kTileRows * SB;
-  // {ring depth, partial buffers}, first that fits. A 4-deep ring (3 tiles in flight per warp,
-  // 60 KB per SM) measured faster than an 8-deep one at one hidden row on GB300 (51.3 vs
-  // 53.5 us): the deeper initial burst delays every warp's first tile.
-  static const int kPlans[][2] = {{4, 4}, {8, 4}, {8, 2}, {4, 2}, {2, 2}};
+  // {ring depth, partial buffers, S/ZS block stages}, first that fits. A 4-deep ring (3 tiles in
+  // flight per warp, 60 KB per SM) measured faster than an 8-deep one at one hidden row on
+  // GB300 (51.3 vs 53.5 us): the deeper initial burst delays every warp's first tile. Two S/ZS
+  // stages make room for 8 hidden rows of the int4 head and of 64-wide groups at K = 5120.
+  static const int kPlans[][3] = {{4, 4, 4}, {8, 4, 4}, {8, 2, 4}, {4, 2, 4}, {4, 2, 2},
+                                  {2, 2, 4}, {2, 2, 2}};
   for (const auto& pl : kPlans) {
-    const int nsw = pl[0], nb = pl[1];
+    const int nsw = pl[0], nb = pl[1], nsb = pl[2];
     if (nsw > nsw_max) continue;
+    int off = 0;
+    a.off_bars = off;
+    off += (kSBlocks + kMaxRedBufs) * 8 + (3 * kMaxRedBufs + kSBlocks + 2) * 4 + 16;
+    a.off_xs = off = (off + 15) / 16 * 16;
+    off += a.NW * 8 * 4 * 4;   // strip group sums: [NW][8 rows][<= 4 groups] fp32
+    off += mt_max * a.KG * 4;  // group sums of the row: [mt][K/G] fp32
+    a.off_zb = off = (off + 15) / 16 * 16;
+    off += (a.KG / 8) * 3 * mt_max * 4 * 8;  // zero-point MMA B fragments: [K/G/8][3][mt][4] uint2
+    a.off_sz = off = (off + 127) / 128 * 128;
+    off += nsb * 2 * kBlockRows * a.KG * 2;
+    a.off_red = off = (off + 15) / 16 * 16;
     const int ring = (a.off_red + nb * red_buf + 127) / 128 * 128;
     if (ring + a.NW * nsw * wstage <= max_smem) {
       a.nb = nb;
+      a.nsb = nsb;
+      a.nsb_log = nsb == 4 ? 2 : 1;
       a.off_ring = ring;
       return nsw;
     }

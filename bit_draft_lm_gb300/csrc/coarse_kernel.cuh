@@ -15,11 +15,11 @@
 //    block stages. The last arrival at the end of block b (an arrival counter: every warp, plus
 //    the zero-point pass) knows that every warp is done with b's stage and partials; it refills
 //    the stage with the S and ZS of the block that
-//    comes kSBlocks later and publishes b's epilogue as one job per hidden row. Warps claim jobs
+//    comes nsb (2 or 4) later and publishes b's epilogue as one job per hidden row. Warps claim jobs
 //    at block boundaries and while they wait (so the fastest warps do them, in parallel): a job
 //    sums the NW partials of its rows in a fixed order (deterministic), selects the top-KCAND
 //    with warp reductions (max key, lowest row on ties) and writes the candidates; the block's
-//    last job releases its partial buffer. A warp waits only when it runs kSBlocks blocks ahead
+//    last job releases its partial buffer. A warp waits only when it runs nsb blocks ahead
 //    of the slowest warp (S stage) or nb blocks ahead of the epilogues (partial buffers).
 //  * Dequant in place, as f16 subnormals: in an f16 pair every bit of the low byte of each half
 //    is mantissa, so for a packed 32-bit word t (bytes b0..b3) the AND of t with the plane's
@@ -65,7 +65,7 @@ namespace dh {
 
 constexpr int kCoarseMaxWarps = 20;  // K <= 5120
 constexpr int kCoarseMaxThreads = kCoarseMaxWarps * 32;
-constexpr int kSBlocks = 4;     // S/ZS block stages
+constexpr int kSBlocks = 4;     // S/ZS block stages at most (the plan picks 4 or 2)
 constexpr int kMaxRedBufs = 4;  // partial buffers (blocks)
 
 struct CoarseArgs {
@@ -86,7 +86,7 @@ struct CoarseArgs {
   // the ALU rate and stalls the tensor pipe's MMAs.)
   uint32_t u16_mul;
   // shared-memory plan
-  int nb, red_pitch;
+  int nb, red_pitch, nsb, nsb_log;  // partial buffers, their row pitch, S/ZS stages (2^nsb_log)
   int off_bars, off_xs, off_zb, off_sz, off_red, off_ring;
 };
 
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   // S and ZS rows of local block lb into stage lb % kSBlocks (rows past N are not copied; the
   // epilogue ignores those rows). One thread.
   auto issue_sz = [&](int lb) {
-    const int st = lb % kSBlocks;
+    const int st = lb & (a.nsb - 1);
     const int row0 = block_row0(lb);
     sz_issued[st] = lb;
     int rows = a.N - row0;
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     *jobs_claimed = 0;
     *abort_flag = 0;
     mbar_fence_init();
-    for (int lb = 0; lb < kSBlocks && lb < my_blocks; ++lb) issue_sz(lb);
+    for (int lb = 0; lb < a.nsb && lb < my_blocks; ++lb) issue_sz(lb);
   }
 
   // ---- weight streaming of tile tau = 4 lb + t into ring stage tau % NSW, by warp `warp` alone:
@@ -595,9 +595,9 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   auto finish_block = [&](int lb, int buf) {
     blk_cnt[buf] = 0;
     __threadfence_block();
-    if (lb + kSBlocks < my_blocks) {
+    if (lb + a.nsb < my_blocks) {
       fence_proxy_async_smem();  // stage reads happen before the copy's writes
-      issue_sz(lb + kSBlocks);
+      issue_sz(lb + a.nsb);
     }
     job_pub[buf] = warp;
     __threadfence_block();
@@ -605,9 +605,9 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   };
 
   for (int lb = 0; lb < my_blocks; ++lb) {
-    const int buf = lb & (nb - 1), sst = lb % kSBlocks;
+    const int buf = lb & (nb - 1), sst = lb & (a.nsb - 1);
     {
-      bool ok = wait_taking_jobs(&full_sb[sst], static_cast<uint32_t>(lb / kSBlocks) & 1u);
+      bool ok = wait_taking_jobs(&full_sb[sst], static_cast<uint32_t>(lb >> a.nsb_log) & 1u);
       if (ok && lb >= nb)
         ok = wait_taking_jobs(&red_empty[buf], static_cast<uint32_t>(lb / nb - 1) & 1u);
       if (!ok) break;
@@ -786,8 +786,8 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
   // memory goes away. (Normally every issued stage has been waited for already.)
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) {
-    for (int q = 0; q < kSBlocks && q < my_blocks; ++q)
-      mbar_wait_bounded(&full_sb[q], static_cast<uint32_t>(sz_issued[q] / kSBlocks) & 1u);
+    for (int q = 0; q < a.nsb && q < my_blocks; ++q)
+      mbar_wait_bounded(&full_sb[q], static_cast<uint32_t>(sz_issued[q] >> a.nsb_log) & 1u);
   }
 }
 

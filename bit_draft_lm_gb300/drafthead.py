@@ -281,29 +281,63 @@ class DraftHead:
         self._am = torch.empty(max_tokens, dtype=torch.int32, device=dev)
 
     def infer(self, x_host: torch.Tensor, stream=None):
-        """End-to-end call from host memory: copies x_host (bf16 [M, K], pinned for an async
-        copy) to the device, runs the head, copies argmax [M], rr_id [M, R] and rr_logit [M, R]
-        back into pinned host tensors and synchronises the stream. Returns those host tensors."""
+        """End-to-end call from host memory: copies x_host (bf16 [M, K]) to the device, runs the
+        head, copies argmax [M], rr_id [M, R] and rr_logit [M, R] back to pinned host memory and
+        synchronises the stream. Returns those host tensors (views of a buffer the next call
+        with the same M overwrites).
+
+        The step is one CUDA graph per M, captured on the first call: the copy in (from a
+        pinned staging buffer that x_host is copied into on the host), the coarse pass, the
+        rerank and one copy out of the three results, which sit in one device buffer."""
         M = x_host.shape[0]
-        if not hasattr(self, "_x_dev") or self._x_dev.shape[0] < M:
-            dev = self.W.device
-            self._x_dev = torch.empty(self.max_tokens, self.K, dtype=torch.bfloat16, device=dev)
-            self._h_am = torch.empty(self.max_tokens, dtype=torch.int32, pin_memory=True)
-            self._h_rr = torch.empty(self.max_tokens, self.rerank, dtype=torch.int32,
-                                     pin_memory=True)
-            self._h_rl = torch.empty(self.max_tokens, self.rerank, dtype=torch.float32,
-                                     pin_memory=True)
+        if M < 1 or M > self.max_tokens:
+            raise ValueError(f"M={M} outside 1..max_tokens={self.max_tokens}")
+        g = self._infer_graphs.get(M) if hasattr(self, "_infer_graphs") else None
+        if g is None:
+            g = self._build_infer_graph(M)
         s = stream if stream is not None else torch.cuda.current_stream()
-        xd = self._x_dev[:M]
+        g["h_x"].copy_(_bf16(x_host, "x_host"))
         with torch.cuda.stream(s):
-            xd.copy_(_bf16(x_host, "x_host"), non_blocking=True)
-            out = self(xd, stream=s)
-            am, rr, rl = self._h_am[:M], self._h_rr[:M], self._h_rl[:M]
-            am.copy_(out["argmax"], non_blocking=True)
-            rr.copy_(out["rr_id"], non_blocking=True)
-            rl.copy_(out["rr_logit"], non_blocking=True)
+            g["graph"].replay()
         s.synchronize()
-        return am, rr, rl
+        return g["h_am"], g["h_rr"], g["h_rl"]
+
+    def _build_infer_graph(self, M: int) -> dict:
+        dev, R = self.W.device, self.rerank
+        g = {"h_x": torch.empty(M, self.K, dtype=torch.bfloat16, pin_memory=True),
+             "d_x": torch.empty(M, self.K, dtype=torch.bfloat16, device=dev),
+             "d_out": torch.empty(M * (1 + 2 * R), dtype=torch.int32, device=dev),
+             "h_out": torch.empty(M * (1 + 2 * R), dtype=torch.int32, pin_memory=True)}
+        d_am = g["d_out"][:M]
+        d_rr = g["d_out"][M:M + M * R].view(M, R)
+        d_rl = g["d_out"][M + M * R:].view(torch.float32).view(M, R)
+        g["h_am"] = g["h_out"][:M]
+        g["h_rr"] = g["h_out"][M:M + M * R].view(M, R)
+        g["h_rl"] = g["h_out"][M + M * R:].view(torch.float32).view(M, R)
+
+        def step():
+            g["d_x"].copy_(g["h_x"], non_blocking=True)
+            cv, ci = dh_draft_head_coarse_topk(g["d_x"], self.packed, self.S, self.ZS, self.N,
+                                               self.G, self.bits, self.kcand,
+                                               cand_val=self._cv[:M], cand_id=self._ci[:M],
+                                               workspace=self.workspace)
+            dh_draft_head_rerank_argmax(g["d_x"], self.W, cv, ci, R, rr_id=d_rr, rr_logit=d_rl,
+                                        argmax_id=d_am, workspace=self.workspace)
+            g["h_out"].copy_(g["d_out"], non_blocking=True)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()  # once outside the capture: first-call set-up of the library
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        g["graph"] = graph
+        if not hasattr(self, "_infer_graphs"):
+            self._infer_graphs = {}
+        self._infer_graphs[M] = g
+        return g
 
     def __call__(self, x: torch.Tensor, y_coarse=None, stream=None):
         """x bf16 [M, K] on the device -> dict of argmax [M], rr_id [M, R], rr_logit [M, R],

@@ -296,3 +296,25 @@ def test_vocabulary_scale_parity(name):
     o_am = oracle.argmax(e_o, o_rr)
     ok = ~near_tie_rows(e_o)
     assert np.array_equal(am.cpu().numpy()[ok], o_am[ok])
+
+
+def test_draft_head_infer_from_host():
+    """DraftHead.infer (one CUDA graph per M: copy in, coarse, rerank, one copy out) returns the
+    same argmax, ids and logits as the device-side call, on successive calls with new inputs and
+    for two row counts."""
+    w = synth.make_workload(3, 1024, 8192, 40, plant=True)
+    W = dev_bf16(w.W)
+    head = dh.DraftHead(W, 128, 2, 8, 16, max_tokens=4)
+    rng = np.random.default_rng(41)
+    for M in (3, 1, 3):
+        for _ in range(2):
+            xs = (rng.standard_normal((M, 1024)) * 1.0).astype(np.float32)
+            x_host = torch.from_numpy(xs).to(torch.bfloat16)
+            am, rr, rl = head.infer(x_host)
+            am, rr, rl = am.clone(), rr.clone(), rl.clone()
+            ref = head(x_host.cuda())
+            torch.cuda.synchronize()
+            assert torch.equal(am, ref["argmax"].cpu())
+            assert torch.equal(rr, ref["rr_id"].cpu())
+            assert torch.equal(rl, ref["rr_logit"].cpu())
+    assert dh.dh_workspace_status(head.workspace) == 0
