@@ -2,6 +2,9 @@
 // No function here allocates device memory or synchronises, except dh_workspace_status.
 #include <cuda_runtime.h>
 
+#include <array>
+#include <mutex>
+
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -105,6 +108,35 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need, const char* who) {
   if (ws_bytes < need)
     return fail(DH_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required", who, ws_bytes, need);
   return DH_OK;
+}
+
+// dh_draft_head_host: per device, a stream of the library's own for capturing (created on first
+// use, kept until exit), and a small cache of captured graphs keyed by every argument.
+struct HostGraphKey {
+  std::array<uint64_t, 24> v;
+};
+struct HostGraph {
+  HostGraphKey key{};
+  cudaGraphExec_t exec = nullptr;
+};
+struct HostDevice {
+  cudaStream_t stream = nullptr;  // where the graphs are captured
+};
+constexpr int kHostGraphs = 16;
+std::mutex g_host_mu;
+HostGraph g_host_graphs[kHostGraphs];
+int g_host_next = 0;
+HostDevice g_host_dev[64];
+
+cudaError_t host_device(int dev, HostDevice** out) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  HostDevice& hd = g_host_dev[dev];
+  if (hd.stream == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&hd.stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  *out = &hd;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -219,6 +251,119 @@ int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void*
   if (e == cudaErrorInvalidValue)
     return fail(DH_ERR_SHAPE, "%s: candidate count does not fit the kernel", who);
   if (e != cudaSuccess) return cuda_fail(e, "rerank_argmax launch");
+  return ok();
+}
+
+int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
+                       const uint8_t* packed, const void* S, const void* ZS, const void* W,
+                       int64_t N, int G, int bits, int kcand, int rerank, float* cand_val,
+                       int32_t* cand_id, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                       int32_t* argmax_host, int32_t* rr_id_host, float* rr_logit_host,
+                       void* workspace, size_t ws_bytes, dh_stream_t s) {
+  const char* who = "draft_head_host";
+  if (!x_host || !x_dev || !argmax_host || !rr_id_host || !rr_logit_host)
+    return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  if (M < 1 || M > DH_MAX_TOKENS || K < 1 || rerank < 1 || rerank > DH_MAX_RERANK)
+    return fail(DH_ERR_SHAPE, "%s: M=%lld K=%lld rerank=%d", who, (long long)M, (long long)K,
+                rerank);
+  if (!aligned(x_dev, 16)) return fail(DH_ERR_ALIGN, "%s: x_dev must be 16-byte aligned", who);
+  cudaStream_t us = reinterpret_cast<cudaStream_t>(s);
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(us, &cap_status);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: stream query");
+  if (cap_status != cudaStreamCaptureStatusNone)
+    return fail(DH_ERR_PARAM, "%s: the stream is being captured (this call synchronises)", who);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: device query");
+
+  // The whole sequence once per distinct argument set and device: captured into a graph on a
+  // stream of the library's own (a capture cannot run on the legacy default stream), then
+  // replayed on s itself.
+  HostGraphKey key{};
+  const uint64_t vals[] = {reinterpret_cast<uint64_t>(x_host), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(K), reinterpret_cast<uint64_t>(x_dev),
+                           reinterpret_cast<uint64_t>(packed), reinterpret_cast<uint64_t>(S),
+                           reinterpret_cast<uint64_t>(ZS), reinterpret_cast<uint64_t>(W),
+                           static_cast<uint64_t>(N), static_cast<uint64_t>(G),
+                           static_cast<uint64_t>(bits), static_cast<uint64_t>(kcand),
+                           static_cast<uint64_t>(rerank), reinterpret_cast<uint64_t>(cand_val),
+                           reinterpret_cast<uint64_t>(cand_id), reinterpret_cast<uint64_t>(rr_id),
+                           reinterpret_cast<uint64_t>(rr_logit),
+                           reinterpret_cast<uint64_t>(argmax_id),
+                           reinterpret_cast<uint64_t>(argmax_host),
+                           reinterpret_cast<uint64_t>(rr_id_host),
+                           reinterpret_cast<uint64_t>(rr_logit_host),
+                           reinterpret_cast<uint64_t>(workspace), static_cast<uint64_t>(ws_bytes),
+                           static_cast<uint64_t>(dev)};
+  static_assert(sizeof(vals) == sizeof(key.v), "key size");
+  for (size_t i = 0; i < sizeof(vals) / sizeof(vals[0]); ++i) key.v[i] = vals[i];
+
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostDevice* hd = nullptr;
+  e = host_device(dev, &hd);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: stream creation");
+  cudaGraphExec_t exec = nullptr;
+  for (auto& c : g_host_graphs)
+    if (c.exec && c.key.v == key.v) exec = c.exec;
+  if (exec == nullptr) {
+    const cudaStream_t cs = hd->stream;
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: begin capture");
+    const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
+    const int64_t ncand = ((N + DH_BLOCK_ROWS - 1) / DH_BLOCK_ROWS) * kcand;
+    const size_t rb = static_cast<size_t>(M) * static_cast<size_t>(rerank) * 4;
+    int rc = DH_OK;
+    e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) {
+      rc = dh_draft_head_coarse_topk(x_dev, M, K, packed, S, ZS, N, G, bits, kcand, cand_val,
+                                     cand_id, nullptr, workspace, ws_bytes,
+                                     reinterpret_cast<dh_stream_t>(cs));
+      if (rc == DH_OK)
+        rc = dh_draft_head_rerank_argmax(x_dev, M, K, W, N, cand_val, cand_id, ncand, rerank,
+                                         rr_id, rr_logit, argmax_id, nullptr, workspace,
+                                         ws_bytes, reinterpret_cast<dh_stream_t>(cs));
+      if (rc == DH_OK) {
+        // one copy when the three results lie back to back on both sides (argmax, rr_id,
+        // rr_logit), else three
+        const size_t ab = static_cast<size_t>(M) * 4;
+        auto* dv = reinterpret_cast<const unsigned char*>(argmax_id);
+        auto* hv = reinterpret_cast<unsigned char*>(argmax_host);
+        const bool joint = reinterpret_cast<const unsigned char*>(rr_id) == dv + ab &&
+                           reinterpret_cast<const unsigned char*>(rr_logit) == dv + ab + rb &&
+                           reinterpret_cast<unsigned char*>(rr_id_host) == hv + ab &&
+                           reinterpret_cast<unsigned char*>(rr_logit_host) == hv + ab + rb;
+        if (joint) {
+          e = cudaMemcpyAsync(hv, dv, ab + 2 * rb, cudaMemcpyDeviceToHost, cs);
+        } else {
+          e = cudaMemcpyAsync(argmax_host, argmax_id, ab, cudaMemcpyDeviceToHost, cs);
+          if (e == cudaSuccess)
+            e = cudaMemcpyAsync(rr_id_host, rr_id, rb, cudaMemcpyDeviceToHost, cs);
+          if (e == cudaSuccess)
+            e = cudaMemcpyAsync(rr_logit_host, rr_logit, rb, cudaMemcpyDeviceToHost, cs);
+        }
+      }
+    }
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ee = cudaStreamEndCapture(cs, &graph);
+    if (rc != DH_OK || e != cudaSuccess || ee != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      if (rc != DH_OK) return rc;  // the failing call recorded its message
+      return cuda_fail(e != cudaSuccess ? e : ee, "draft_head_host: capture");
+    }
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: instantiate");
+    HostGraph& slot = g_host_graphs[g_host_next];
+    g_host_next = (g_host_next + 1) % kHostGraphs;
+    if (slot.exec) cudaGraphExecDestroy(slot.exec);  // the oldest argument set
+    slot.key = key;
+    slot.exec = exec;
+  }
+  e = cudaGraphLaunch(exec, us);  // stream-ordered after the caller's earlier work on s
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: launch");
+  e = cudaStreamSynchronize(us);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: synchronise");
   return ok();
 }
 

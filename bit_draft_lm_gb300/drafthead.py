@@ -45,6 +45,8 @@ SIGNATURES = {
                                      _P, _SZ, _P], _I),
     "dh_draft_head_rerank_argmax_noalloc": ([_P, _I64, _I64, _P, _I64, _P, _P, _I64, _I, _P,
                                              _P, _P, _P, _P], _I),
+    "dh_draft_head_host": ([_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
+                            _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "dh_workspace_status": ([_P, _SZ, _P, _P], _I),
     "dh_last_error": ([], ctypes.c_char_p),
 }
@@ -301,6 +303,45 @@ class DraftHead:
             g["graph"].replay()
         s.synchronize()
         return g["h_am"], g["h_rr"], g["h_rl"]
+
+    def call_host(self, x_host: torch.Tensor, stream=None):
+        """The same end-to-end call through the library's host-memory entry point
+        (dh_draft_head_host): copy in, coarse pass, rerank, copies out and the synchronisation
+        all happen in native code. Returns pinned host tensors (argmax [M], rr_id [M, R],
+        rr_logit [M, R]), views of buffers the next call with the same M overwrites."""
+        M, R = x_host.shape[0], self.rerank
+        sh = _stream(stream)
+        key = (M, x_host.data_ptr(), sh)
+        cached = self._host_calls.get(key) if hasattr(self, "_host_calls") else None
+        if cached is None:
+            if M < 1 or M > self.max_tokens:
+                raise ValueError(f"M={M} outside 1..max_tokens={self.max_tokens}")
+            xb = _bf16(x_host, "x_host")
+            if xb.is_cuda or not xb.is_contiguous() or tuple(xb.shape) != (M, self.K):
+                raise ValueError("x_host must be a contiguous host tensor [M, K]")
+            if not hasattr(self, "_host_bufs"):
+                dev, n = self.W.device, self.max_tokens * (1 + 2 * R)
+                # results back to back (argmax, rr_id, rr_logit) on both sides: one copy out
+                self._host_bufs = (
+                    torch.empty(self.max_tokens, self.K, dtype=torch.bfloat16, device=dev),
+                    torch.empty(n, dtype=torch.int32, device=dev),
+                    torch.empty(n, dtype=torch.int32, pin_memory=True))
+                self._host_calls = {}
+            x_dev, d_out, h_out = self._host_bufs
+            d_am, d_rr, d_rl = d_out[:M], d_out[M:M + M * R], d_out[M + M * R:M + 2 * M * R]
+            h_am = h_out[:M]
+            h_rr = h_out[M:M + M * R].view(M, R)
+            h_rl = h_out[M + M * R:M + 2 * M * R].view(torch.float32).view(M, R)
+            ws = self.workspace
+            args = (xb.data_ptr(), M, self.K, x_dev.data_ptr(), self.packed.data_ptr(),
+                    self.S.data_ptr(), self.ZS.data_ptr(), self.W.data_ptr(), self.N, self.G,
+                    self.bits, self.kcand, R, self._cv.data_ptr(), self._ci.data_ptr(),
+                    d_rr.data_ptr(), d_rl.data_ptr(), d_am.data_ptr(), h_am.data_ptr(),
+                    h_rr.data_ptr(), h_rl.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+            cached = (args, (h_am, h_rr, h_rl), x_host)  # x_host kept alive with its pointer
+            self._host_calls[key] = cached
+        _check(lib().dh_draft_head_host(*cached[0]))
+        return cached[1]
 
     def _build_infer_graph(self, M: int) -> dict:
         dev, R = self.W.device, self.rerank

@@ -17,8 +17,9 @@
  *  - Calls are asynchronous and stream-ordered on `s` (NULL = the legacy default stream). The
  *    return value reports argument validation and launch errors only (cudaGetLastError is read
  *    without synchronising); failures detected inside a kernel are recorded in the workspace
- *    status word (see dh_workspace_status). No call synchronises the device or allocates, so
- *    the per-call entry points can be captured in a CUDA graph.
+ *    status word (see dh_workspace_status). No call allocates device memory, and none but
+ *    dh_workspace_status and dh_draft_head_host synchronises, so the per-call device entry
+ *    points can be captured in a CUDA graph.
  *  - On any non-OK return nothing was launched; dh_last_error() gives a message.
  *  - Pointers read with 16-byte vector loads must be 16-byte aligned (DH_ERR_ALIGN otherwise).
  */
@@ -164,6 +165,26 @@ int dh_draft_head_rerank_argmax_noalloc(const void* x, int64_t M, int64_t K, con
                                         int64_t ncand, int rerank, int32_t* rr_id,
                                         float* rr_logit, int32_t* argmax_id, void* y_coarse,
                                         dh_stream_t s);
+
+/*
+ * The whole call from and to host memory (_apply_head_int2 end to end): copies x_host (bf16
+ * [M, K]) into x_dev, runs dh_draft_head_coarse_topk and dh_draft_head_rerank_argmax, copies
+ * argmax [M], rr_id [M, rerank] and rr_logit [M, rerank] back into argmax_host, rr_id_host and
+ * rr_logit_host, and synchronises (the one call besides dh_workspace_status that does).
+ * x_host and the three host arrays must be page-locked (pinned) memory.
+ *   x_dev, cand_val, cand_id, rr_id, rr_logit, argmax_id, workspace: device buffers as for the
+ *   two calls it makes (their device outputs are written too); the other arguments likewise.
+ * The sequence is captured into a CUDA graph the first time an argument set is seen on a
+ * device (on a stream of the library's own) and replayed on s on later calls. The library
+ * keeps the 16 most recent such graphs and one capture stream per device, no device memory. Returns DH_ERR_PARAM while s is being captured; otherwise the first failing step's
+ * status. A kernel-side failure is read with dh_workspace_status.
+ */
+int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
+                       const uint8_t* packed, const void* S, const void* ZS, const void* W,
+                       int64_t N, int G, int bits, int kcand, int rerank, float* cand_val,
+                       int32_t* cand_id, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                       int32_t* argmax_host, int32_t* rr_id_host, float* rr_logit_host,
+                       void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
  * Synchronises `s`, copies the workspace status word to *device_status and returns DH_OK if

@@ -318,3 +318,24 @@ def test_draft_head_infer_from_host():
             assert torch.equal(rr, ref["rr_id"].cpu())
             assert torch.equal(rl, ref["rr_logit"].cpu())
     assert dh.dh_workspace_status(head.workspace) == 0
+
+
+def test_draft_head_host_entry_point():
+    """dh_draft_head_host (copy in, coarse, rerank, copies out, synchronise, all native) returns
+    the same results as the device-side call and as the graph-replayed infer."""
+    w = synth.make_workload(2, 1024, 8192, 42, plant=True)
+    W = dev_bf16(w.W)
+    head = dh.DraftHead(W, 128, 2, 8, 16, max_tokens=2)
+    rng = np.random.default_rng(43)
+    for M in (2, 1, 2):
+        xs = rng.standard_normal((M, 1024)).astype(np.float32)
+        x_host = torch.from_numpy(xs).to(torch.bfloat16).pin_memory()
+        am, rr, rl = (t.clone() for t in head.call_host(x_host))
+        ref = head(x_host.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(am, ref["argmax"].cpu())
+        assert torch.equal(rr, ref["rr_id"].cpu())
+        assert torch.equal(rl, ref["rr_logit"].cpu())
+        gam, grr, grl = head.infer(x_host)
+        assert torch.equal(am, gam) and torch.equal(rr, grr) and torch.equal(rl, grl)
+    assert dh.dh_workspace_status(head.workspace) == 0
