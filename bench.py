@@ -157,7 +157,8 @@ def run_ours(args, rank, world):
     dh_build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    xs_h, W_h = workload_host(max([args.m] + extra_ms(args)))
+    # rows of x for every measured workload (the variant lines use 8)
+    xs_h, W_h = workload_host(max([args.m] + extra_ms(args) + ([] if args.no_variants else [8])))
     W0 = torch.from_numpy(W_h.view(np.int16)).to(dev).view(torch.bfloat16)
     ncopy = max(1, args.copies)
     Ws = [W0] + [W0.clone() for _ in range(ncopy - 1)]
@@ -165,7 +166,8 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     nblk = (N_VOCAB + 63) // 64
 
-    def measure(M, steps, warmup, record_launches, bits=2, group=GROUP, kcand=KCAND, packs=packs):
+    def measure(M, steps, warmup, record_launches, bits=2, group=GROUP, kcand=KCAND, packs=packs,
+                fp8_rows=None):
         xs = [torch.from_numpy(xs_h[c, :M].copy().view(np.int16)).to(dev).view(torch.bfloat16)
               for c in range(ncopy)]
         ws = dh.new_workspace(M, N_VOCAB, K_DIM, kcand, RERANK, dev)
@@ -180,7 +182,11 @@ def run_ours(args, rank, world):
             p, S, ZS = packs[c]
             dh.dh_draft_head_coarse_topk(xs[c], p, S, ZS, N_VOCAB, group, bits, kcand,
                                          cand_val=cv, cand_id=ci, workspace=ws)
-            if not coarse_only:
+            if not coarse_only and fp8_rows is not None:
+                dh.dh_draft_head_rerank_argmax_fp8(xs[c], fp8_rows[c][0], fp8_rows[c][1], cv, ci,
+                                                   RERANK, rr_id=rr, rr_logit=rl, argmax_id=am,
+                                                   workspace=ws)
+            elif not coarse_only:
                 dh.dh_draft_head_rerank_argmax(xs[c], Ws[c], cv, ci, RERANK, rr_id=rr,
                                                rr_logit=rl, argmax_id=am, workspace=ws)
 
@@ -283,6 +289,24 @@ def run_ours(args, rank, world):
                               "hbm_gbs_per_call": round(alg / u / 1e3, 1), "steps": steps}
             del vp
             torch.cuda.synchronize()
+        # the FP8 checkpoint's head at M=1: int2 codes quantised from e4m3 rows x row scale, the
+        # rerank against the e4m3 rows (half the gather bytes of bf16 rows)
+        from bit_draft_lm_gb300 import synth
+        w8h, sch = synth.fp8_head(W_h)
+        rows = [(torch.from_numpy(w8h).to(dev), torch.from_numpy(sch).to(dev))
+                for _ in range(ncopy)]
+        vp = [dh.dh_quantize_pack_int2_fp8(r[0], r[1], GROUP) for r in rows]
+        steps = max(50, min(args.steps, 1000))
+        mm, cm = measure(1, steps, 8, True, packs=vp, fp8_rows=rows)
+        u = mm * 1e3 / steps
+        alg = alg_coarse + RERANK * K_DIM
+        variants["fp8_head_m1_kcand8"] = {"us_per_call": round(u, 3),
+                                          "coarse_us": round(1e3 * cm / steps, 3),
+                                          "algorithmic_bytes_per_call": alg,
+                                          "hbm_gbs_per_call": round(alg / u / 1e3, 1),
+                                          "steps": steps}
+        del vp, rows
+        torch.cuda.synchronize()
 
     e2e = None
     if not args.no_e2e:

@@ -149,6 +149,39 @@ int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
 size_t rerank_workspace_needed() { return rerank_workspace_bytes(); }
 }  // namespace dh
 
+static int rerank_impl(const char* who, const void* x, int64_t M, int64_t K, const void* W,
+                       const uint8_t* W8, const float* wscale, int64_t N,
+                                const float* cand_val, const int32_t* cand_id, int64_t ncand,
+                                int rerank, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                                void* y_coarse, void* workspace, size_t ws_bytes,
+                                dh_stream_t s) {
+  if (!x || (!W && !W8) || (W8 && !wscale) || !cand_val || !cand_id || !rr_id || !rr_logit || !argmax_id)
+    return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  if (rerank < 1 || rerank > DH_MAX_RERANK)
+    return fail(DH_ERR_PARAM, "%s: rerank=%d (1..%d)", who, rerank, DH_MAX_RERANK);
+  if (M < 1 || M > DH_MAX_TOKENS)
+    return fail(DH_ERR_SHAPE, "%s: M=%lld (1..%d)", who, (long long)M, DH_MAX_TOKENS);
+  if (N < 1 || N > (int64_t)INT32_MAX || K < 8 || K % 8 || K > 32768)
+    return fail(DH_ERR_SHAPE, "%s: N=%lld K=%lld (K a multiple of 8, at most 32768)", who,
+                (long long)N, (long long)K);
+  if (ncand < rerank || ncand > (int64_t)1 << 20)
+    return fail(DH_ERR_SHAPE, "%s: ncand=%lld must be in [rerank, 2^20]", who, (long long)ncand);
+  if (!aligned(x, 16) || !aligned(W ? W : W8, 16) || (wscale && !aligned(wscale, 4)))
+    return fail(DH_ERR_ALIGN, "%s: x and W must be 16-byte aligned", who);
+  if (!aligned(cand_val, 4) || !aligned(cand_id, 4) || !aligned(rr_id, 4) ||
+      !aligned(rr_logit, 4) || !aligned(argmax_id, 4) || (y_coarse && !aligned(y_coarse, 2)))
+    return fail(DH_ERR_ALIGN, "%s: misaligned candidate or output array", who);
+  int rc = check_workspace(workspace, ws_bytes, rerank_workspace_bytes(), who);
+  if (rc != DH_OK) return rc;
+  dh::RerankCall r{x, M, K, W, N, cand_val, cand_id, ncand, rerank, rr_id, rr_logit, argmax_id,
+                   y_coarse, static_cast<uint32_t*>(workspace), W8, wscale};
+  cudaError_t e = dh::launch_rerank_argmax(r, reinterpret_cast<cudaStream_t>(s));
+  if (e == cudaErrorInvalidValue)
+    return fail(DH_ERR_SHAPE, "%s: candidate count does not fit the kernel", who);
+  if (e != cudaSuccess) return cuda_fail(e, "rerank_argmax launch");
+  return ok();
+}
+
 extern "C" {
 
 int dh_quantize_pack_int2(const void* W, int64_t N, int64_t K, int G, uint8_t* packed, void* S,
@@ -159,6 +192,18 @@ int dh_quantize_pack_int2(const void* W, int64_t N, int64_t K, int G, uint8_t* p
 int dh_quantize_pack_int4(const void* W, int64_t N, int64_t K, int G, uint8_t* packed, void* S,
                           void* ZS, dh_stream_t s) {
   return quantize(4, W, N, K, G, packed, S, ZS, s);
+}
+
+int dh_quantize_pack_int2_fp8(const uint8_t* W8, const float* row_scale, int64_t N, int64_t K,
+                              int G, uint8_t* packed, void* S, void* ZS, dh_stream_t s) {
+  int rc = check_quant(W8, N, K, G, packed, S, ZS, 2);
+  if (rc != DH_OK) return rc;
+  if (!row_scale) return fail(DH_ERR_NULL, "quantize_pack_int2_fp8: row_scale is NULL");
+  if (!aligned(row_scale, 4)) return fail(DH_ERR_ALIGN, "quantize_pack_int2_fp8: row_scale");
+  cudaError_t e = dh::launch_quantize_pack(2, W8, N, K, G, packed, S, ZS,
+                                           reinterpret_cast<cudaStream_t>(s), row_scale);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize_pack_int2_fp8 launch");
+  return ok();
 }
 
 size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits) {
@@ -226,31 +271,37 @@ int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void*
                                 int rerank, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
                                 void* y_coarse, void* workspace, size_t ws_bytes,
                                 dh_stream_t s) {
-  const char* who = "draft_head_rerank_argmax";
-  if (!x || !W || !cand_val || !cand_id || !rr_id || !rr_logit || !argmax_id)
-    return fail(DH_ERR_NULL, "%s: NULL pointer", who);
-  if (rerank < 1 || rerank > DH_MAX_RERANK)
-    return fail(DH_ERR_PARAM, "%s: rerank=%d (1..%d)", who, rerank, DH_MAX_RERANK);
-  if (M < 1 || M > DH_MAX_TOKENS)
-    return fail(DH_ERR_SHAPE, "%s: M=%lld (1..%d)", who, (long long)M, DH_MAX_TOKENS);
-  if (N < 1 || N > (int64_t)INT32_MAX || K < 8 || K % 8 || K > 32768)
-    return fail(DH_ERR_SHAPE, "%s: N=%lld K=%lld (K a multiple of 8, at most 32768)", who,
-                (long long)N, (long long)K);
-  if (ncand < rerank || ncand > (int64_t)1 << 20)
-    return fail(DH_ERR_SHAPE, "%s: ncand=%lld must be in [rerank, 2^20]", who, (long long)ncand);
-  if (!aligned(x, 16) || !aligned(W, 16))
-    return fail(DH_ERR_ALIGN, "%s: x and W must be 16-byte aligned", who);
-  if (!aligned(cand_val, 4) || !aligned(cand_id, 4) || !aligned(rr_id, 4) ||
-      !aligned(rr_logit, 4) || !aligned(argmax_id, 4) || (y_coarse && !aligned(y_coarse, 2)))
-    return fail(DH_ERR_ALIGN, "%s: misaligned candidate or output array", who);
-  int rc = check_workspace(workspace, ws_bytes, rerank_workspace_bytes(), who);
-  if (rc != DH_OK) return rc;
-  dh::RerankCall r{x, M, K, W, N, cand_val, cand_id, ncand, rerank, rr_id, rr_logit, argmax_id,
-                   y_coarse, static_cast<uint32_t*>(workspace)};
-  cudaError_t e = dh::launch_rerank_argmax(r, reinterpret_cast<cudaStream_t>(s));
-  if (e == cudaErrorInvalidValue)
-    return fail(DH_ERR_SHAPE, "%s: candidate count does not fit the kernel", who);
-  if (e != cudaSuccess) return cuda_fail(e, "rerank_argmax launch");
+  if (!W) return fail(DH_ERR_NULL, "draft_head_rerank_argmax: NULL pointer");
+  return rerank_impl("draft_head_rerank_argmax", x, M, K, W, nullptr, nullptr, N, cand_val,
+                     cand_id, ncand, rerank, rr_id, rr_logit, argmax_id, y_coarse, workspace,
+                     ws_bytes, s);
+}
+
+int dh_draft_head_rerank_argmax_fp8(const void* x, int64_t M, int64_t K, const uint8_t* W8,
+                                    const float* row_scale, int64_t N, const float* cand_val,
+                                    const int32_t* cand_id, int64_t ncand, int rerank,
+                                    int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                                    void* y_coarse, void* workspace, size_t ws_bytes,
+                                    dh_stream_t s) {
+  if (!W8 || !row_scale) return fail(DH_ERR_NULL, "draft_head_rerank_argmax_fp8: NULL pointer");
+  return rerank_impl("draft_head_rerank_argmax_fp8", x, M, K, nullptr, W8, row_scale, N,
+                     cand_val, cand_id, ncand, rerank, rr_id, rr_logit, argmax_id, y_coarse,
+                     workspace, ws_bytes, s);
+}
+
+int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
+                        int64_t N, void* y, dh_stream_t s) {
+  const char* who = "topk_only_logits";
+  if (!rr_id || !rr_logit || !y) return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  if (M < 1 || M > DH_MAX_TOKENS || N < 1 || N > (int64_t)INT32_MAX || rerank < 1 ||
+      rerank > DH_MAX_RERANK)
+    return fail(DH_ERR_SHAPE, "%s: M=%lld N=%lld rerank=%d", who, (long long)M, (long long)N,
+                rerank);
+  if (!aligned(rr_id, 4) || !aligned(rr_logit, 4) || !aligned(y, 2))
+    return fail(DH_ERR_ALIGN, "%s: misaligned array", who);
+  cudaError_t e = dh::launch_topk_only(rr_id, rr_logit, M, rerank, N, y,
+                                       reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "topk_only_logits launch");
   return ok();
 }
 

@@ -36,10 +36,15 @@ struct RerankCall {
   int32_t* argmax_id;
   void* y;
   uint32_t* status;
+  const uint8_t* W8 = nullptr;      // e4m3 rows [N, K] instead of W (FP8 checkpoints) ...
+  const float* wscale = nullptr;    // ... with their fp32 per-row scale [N]
 };
 
+// W bf16 [N, K], or (row_scale != nullptr) e4m3 [N, K] bytes whose values are multiplied by the
+// fp32 per-row scale before quantising.
 cudaError_t launch_quantize_pack(int bits, const void* W, int64_t N, int64_t K, int G,
-                                 uint8_t* packed, void* S, void* ZS, cudaStream_t s);
+                                 uint8_t* packed, void* S, void* ZS, cudaStream_t s,
+                                 const float* row_scale = nullptr);
 // cudaErrorInvalidValue: the shape does not fit the kernel's shared-memory plan.
 cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s);
 // The tensor-core (tcgen05) pass of int2 heads for more than kWideMinRows hidden rows, up to
@@ -52,6 +57,9 @@ bool coarse_wide_supports(const CoarseCall& cc);
 cudaError_t launch_coarse_wide(const CoarseCall& cc, void* scratch, int num_sms, int max_smem,
                                cudaStream_t s);
 cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s);
+// y [M, N] bf16 = -inf except y[m, rr_id[m, j]] = bf16(rr_logit[m, j]) (topk_only.cu).
+cudaError_t launch_topk_only(const int32_t* rr_id, const float* rr_logit, int64_t M, int R,
+                             int64_t N, void* y, cudaStream_t s);
 // Sets the calling thread's dh_last_error() message; returns `code`.
 int record_error(int code, const char* msg);
 // Workspace bytes dh_draft_head_rerank_argmax requires (independent of the sizes).

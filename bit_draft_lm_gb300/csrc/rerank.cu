@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "dh_device.cuh"
 #include "dh_launch.h"
@@ -33,7 +34,9 @@ constexpr int kRerankWarps = kRerankThreads / 32;
 struct RerankArgs {
   const uint16_t* x;  // bf16 [M, K]
   int K, N;
-  const uint16_t* W;  // bf16 [N, K]
+  const uint16_t* W;  // bf16 [N, K] (bf16 rows)
+  const uint8_t* W8;  // e4m3 [N, K] (FP8 rows) ...
+  const float* wscale;  // ... and their fp32 per-row scale [N]
   const float* cand_val;  // [M, ncand]
   const int32_t* cand_id;
   int ncand, R;
@@ -88,16 +91,56 @@ __device__ __forceinline__ Sel warp_sort(Sel v) {
 constexpr int kSurvivorCap = 256;  // candidates the one-warp exact selection takes after the filter
 constexpr int kRerankUnroll = 8;   // weight-row loads each lane keeps in flight
 
-// 16-byte load through the read-only (non-coherent) path: W is never written by the library.
+// 8 weights of a row, k = 8 k8 .. 8 k8 + 7: 16 bytes of bf16 or 8 bytes of e4m3.
+template <bool FP8>
+struct Row8 {
+  using Raw = typename std::conditional<FP8, uint2, uint4>::type;
+};
+__device__ __forceinline__ uint2 ldg_nc_v2(const uint2* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+// Weight pair q (k = 8 k8 + 2q, + 1) of 8 loaded weights, as fp32 (exact).
+__device__ __forceinline__ void w_pair(const uint4& w, int q, float& lo, float& hi) {
+  const uint32_t v = q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
+  lo = __uint_as_float(v << 16);
+  hi = __uint_as_float(v & 0xffff0000u);
+}
+// e4m3 bytes: the page's exact bit decode (e4m3_to_f32), no hardware conversion.
+__device__ __forceinline__ void w_pair(const uint2& w, int q, float& lo, float& hi) {
+  const uint32_t v = q < 2 ? w.x : w.y;
+  const int sh = 16 * (q & 1);
+  lo = e4m3_to_f32((v >> sh) & 0xffu);
+  hi = e4m3_to_f32((v >> (sh + 8)) & 0xffu);
+}
+template <bool FP8>
+__device__ __forceinline__ typename Row8<FP8>::Raw load_w8(const RerankArgs& a, int n, int k8);
+
+// Loads through the read-only (non-coherent) path: W is never written by the library.
 __device__ __forceinline__ uint4 ldg_nc_v4(const uint4* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}  // candidates the one-warp exact selection takes after the filter
+}
 
-template <int LPT>
+template <>
+__device__ __forceinline__ uint4 load_w8<false>(const RerankArgs& a, int n, int k8) {
+  return ldg_nc_v4(reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(n) * a.K) + k8);
+}
+template <>
+__device__ __forceinline__ uint2 load_w8<true>(const RerankArgs& a, int n, int k8) {
+  return ldg_nc_v2(reinterpret_cast<const uint2*>(a.W8 + static_cast<int64_t>(n) * a.K) + k8);
+}
+// The factor the row's dot is multiplied by: 1 for bf16 rows, the per-row scale for e4m3 rows.
+template <bool FP8>
+__device__ __forceinline__ float row_scale(const RerankArgs& a, int n) {
+  return FP8 ? a.wscale[n] : 1.0f;
+}
+
+template <int LPT, bool FP8>
 __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const RerankArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(sm);                      // [K]
@@ -267,36 +310,37 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
     const int n = sel_id[j];
     float logit = -INFINITY;
     if (n >= 0 && n < a.N) {
-      const uint4* wr = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(n) * a.K);
       const uint4* xr = reinterpret_cast<const uint4*>(xs);
       float acc = 0.0f;
       const int k8_end = min(a.K / 8, (part + 1) * k8_per);
-      // kRerankUnroll 16-byte loads of the weight row in flight per lane before any is used
+      // kRerankUnroll loads of the weight row (16 bytes of bf16 or 8 of e4m3 each) in flight
+      // per lane before any is used
       for (int k8b = part * k8_per + lane; k8b < k8_end; k8b += 32 * kRerankUnroll) {
-        uint4 w8[kRerankUnroll];
+        typename Row8<FP8>::Raw w8[kRerankUnroll];
 #pragma unroll
         for (int u = 0; u < kRerankUnroll; ++u) {
           const int k8 = k8b + 32 * u;
-          w8[u] = k8 < k8_end ? ldg_nc_v4(wr + k8) : make_uint4(0u, 0u, 0u, 0u);
+          w8[u] = load_w8<FP8>(a, n, k8 < k8_end ? k8 : part * k8_per);
         }
 #pragma unroll
         for (int u = 0; u < kRerankUnroll; ++u) {
           const int k8 = k8b + 32 * u;
           if (k8 < k8_end) {
             const uint4 x8 = xr[k8];
-            const uint32_t wv[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
             const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
             float part = 0.0f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              part = fmaf(__uint_as_float(xv[q] << 16), __uint_as_float(wv[q] << 16), part);
-              part = fmaf(__uint_as_float(xv[q] & 0xffff0000u),
-                          __uint_as_float(wv[q] & 0xffff0000u), part);
+              float wl, wh;
+              w_pair(w8[u], q, wl, wh);
+              part = fmaf(__uint_as_float(xv[q] << 16), wl, part);
+              part = fmaf(__uint_as_float(xv[q] & 0xffff0000u), wh, part);
             }
             acc += part;
           }
         }
       }
+      acc *= row_scale<FP8>(a, n);
 #pragma unroll
       for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       logit = acc;
@@ -376,7 +420,7 @@ __device__ __forceinline__ T* cta0(cg::cluster_group& cl, T* p) {
   return cl.map_shared_rank(p, 0);
 }
 
-template <int LPT>
+template <int LPT, bool FP8>
 __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     rerank_cluster_kernel(const RerankArgs a) {
   cg::cluster_group cl = cg::this_cluster();
@@ -532,22 +576,23 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     const int k8n = a.K / 8;
     const uint4* xr = reinterpret_cast<const uint4*>(xs);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const uint4* wr[4];
+    int rown[4];
     bool live[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int n = u < nslot ? sh.rr[rank + u * kRC] : -1;
       live[u] = n >= 0 && n < a.N;
-      wr[u] = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(live[u] ? n : 0) * a.K);
+      rown[u] = live[u] ? n : 0;
     }
     for (int k8b = tid; k8b < k8n; k8b += kRCThreads * 3) {
-      uint4 w8[4][3];
+      typename Row8<FP8>::Raw w8[4][3];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           const int k8 = k8b + q * kRCThreads;
-          w8[u][q] = live[u] && k8 < k8n ? ldg_nc_v4(wr[u] + k8) : make_uint4(0u, 0u, 0u, 0u);
+          if (live[u] && k8 < k8n) w8[u][q] = load_w8<FP8>(a, rown[u], k8);
+          else w8[u][q] = {};
         }
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
@@ -557,18 +602,21 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
           const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t wv[4] = {w8[u][q].x, w8[u][q].y, w8[u][q].z, w8[u][q].w};
             float p = 0.0f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              p = fmaf(__uint_as_float(xv[e] << 16), __uint_as_float(wv[e] << 16), p);
-              p = fmaf(__uint_as_float(xv[e] & 0xffff0000u), __uint_as_float(wv[e] & 0xffff0000u), p);
+              float wl, wh;
+              w_pair(w8[u][q], e, wl, wh);
+              p = fmaf(__uint_as_float(xv[e] << 16), wl, p);
+              p = fmaf(__uint_as_float(xv[e] & 0xffff0000u), wh, p);
             }
             acc[u] += p;
           }
         }
       }
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] *= live[u] ? row_scale<FP8>(a, rown[u]) : 1.0f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
 #pragma unroll
@@ -613,10 +661,10 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
   }
 }
 
-template <int LPT>
+template <int LPT, bool FP8>
 static cudaError_t launch_rc(const RerankArgs& a, int M, cudaStream_t s) {
   const int smem = 2 * a.K;
-  cudaError_t e = cudaFuncSetAttribute(rerank_cluster_kernel<LPT>,
+  cudaError_t e = cudaFuncSetAttribute(rerank_cluster_kernel<LPT, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the CTAs may start (and stage x) while the kernel before
@@ -631,23 +679,42 @@ static cudaError_t launch_rc(const RerankArgs& a, int M, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, rerank_cluster_kernel<LPT>, a);
+  e = cudaLaunchKernelEx(&cfg, rerank_cluster_kernel<LPT, FP8>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int LPT>
+template <int LPT, bool FP8>
 static cudaError_t launch_rr(const RerankArgs& a, int M, cudaStream_t s) {
   size_t smem = static_cast<size_t>(2 * a.K) + sizeof(Sel) * (kRerankWarps + 1) +
                 static_cast<size_t>(a.R) * 8 + static_cast<size_t>(a.R) * kRerankWarps * 4 +
                 sizeof(Sel) * kSurvivorCap + 4 * (kRerankWarps + 2);
   if (LPT == 0) smem += 4 * static_cast<size_t>((a.ncand + 31) / 32);
-  cudaError_t e = cudaFuncSetAttribute(rerank_argmax_kernel<LPT>,
+  cudaError_t e = cudaFuncSetAttribute(rerank_argmax_kernel<LPT, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  rerank_argmax_kernel<LPT><<<M, kRerankThreads, smem, s>>>(a);
+  rerank_argmax_kernel<LPT, FP8><<<M, kRerankThreads, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <bool FP8>
+static cudaError_t launch_rerank_fmt(const RerankArgs& a, const RerankCall& rc, cudaStream_t s) {
+  const int M = static_cast<int>(rc.M);
+  if (rc.R <= kRCMaxR && rc.ncand <= kRCMaxCand && rc.K <= 32768) {
+    const int64_t lpt = ((rc.ncand + kRC - 1) / kRC + kRCThreads - 1) / kRCThreads;
+    if (lpt <= 1) return launch_rc<1, FP8>(a, M, s);
+    if (lpt <= 2) return launch_rc<2, FP8>(a, M, s);
+    if (lpt <= 4) return launch_rc<4, FP8>(a, M, s);
+    return launch_rc<8, FP8>(a, M, s);
+  }
+  const int64_t per = (rc.ncand + kRerankThreads - 1) / kRerankThreads;
+  if (per <= 1) return launch_rr<1, FP8>(a, M, s);
+  if (per <= 2) return launch_rr<2, FP8>(a, M, s);
+  if (per <= 4) return launch_rr<4, FP8>(a, M, s);
+  if (per <= 8) return launch_rr<8, FP8>(a, M, s);
+  if (per <= 16) return launch_rr<16, FP8>(a, M, s);
+  return launch_rr<0, FP8>(a, M, s);
 }
 
 cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s) {
@@ -656,6 +723,8 @@ cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s) {
   a.K = static_cast<int>(rc.K);
   a.N = static_cast<int>(rc.N);
   a.W = static_cast<const uint16_t*>(rc.W);
+  a.W8 = rc.W8;
+  a.wscale = rc.wscale;
   a.cand_val = rc.cand_val;
   a.cand_id = rc.cand_id;
   a.ncand = static_cast<int>(rc.ncand);
@@ -665,21 +734,7 @@ cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s) {
   a.argmax_id = rc.argmax_id;
   a.y = static_cast<uint16_t*>(rc.y);
   a.status = rc.status;
-  const int M = static_cast<int>(rc.M);
-  if (rc.R <= kRCMaxR && rc.ncand <= kRCMaxCand && rc.K <= 32768) {
-    const int64_t lpt = ((rc.ncand + kRC - 1) / kRC + kRCThreads - 1) / kRCThreads;
-    if (lpt <= 1) return launch_rc<1>(a, M, s);
-    if (lpt <= 2) return launch_rc<2>(a, M, s);
-    if (lpt <= 4) return launch_rc<4>(a, M, s);
-    return launch_rc<8>(a, M, s);
-  }
-  const int64_t per = (rc.ncand + kRerankThreads - 1) / kRerankThreads;
-  if (per <= 1) return launch_rr<1>(a, M, s);
-  if (per <= 2) return launch_rr<2>(a, M, s);
-  if (per <= 4) return launch_rr<4>(a, M, s);
-  if (per <= 8) return launch_rr<8>(a, M, s);
-  if (per <= 16) return launch_rr<16>(a, M, s);
-  return launch_rr<0>(a, M, s);
+  return rc.W8 != nullptr ? launch_rerank_fmt<true>(a, rc, s) : launch_rerank_fmt<false>(a, rc, s);
 }
 
 }  // namespace dh

@@ -47,6 +47,10 @@ SIGNATURES = {
                                              _P, _P, _P, _P], _I),
     "dh_draft_head_host": ([_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
                             _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "dh_topk_only_logits": ([_P, _P, _I64, _I, _I64, _P, _P], _I),
+    "dh_quantize_pack_int2_fp8": ([_P, _P, _I64, _I64, _I, _P, _P, _P, _P], _I),
+    "dh_draft_head_rerank_argmax_fp8": ([_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _I, _P, _P,
+                                         _P, _P, _P, _SZ, _P], _I),
     "dh_workspace_status": ([_P, _SZ, _P, _P], _I),
     "dh_last_error": ([], ctypes.c_char_p),
 }
@@ -247,6 +251,72 @@ def dh_draft_head_rerank_argmax_noalloc(x: torch.Tensor, W: torch.Tensor,
         _dev(argmax_id, "argmax_id", torch.int32, (M,)),
         _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)), _stream(stream)))
     return rr_id, rr_logit, argmax_id
+
+
+def dh_quantize_pack_int2_fp8(W8: torch.Tensor, row_scale: torch.Tensor, G: int = 128,
+                              packed=None, S=None, ZS=None, stream=None):
+    """FP8 head (e4m3 rows [N, K] as uint8 or float8_e4m3fn, fp32 per-row scale [N]) ->
+    (packed, S, ZS) of the values e4m3 * scale."""
+    if W8.dtype == torch.float8_e4m3fn:
+        W8 = W8.view(torch.uint8)
+    N, K = W8.shape
+    dev = W8.device
+    if packed is None:
+        packed = torch.empty(N, K // 4, dtype=torch.uint8, device=dev)
+    if S is None:
+        S = torch.empty(N, K // G, dtype=torch.bfloat16, device=dev)
+    if ZS is None:
+        ZS = torch.empty(N, K // G, dtype=torch.bfloat16, device=dev)
+    _check(lib().dh_quantize_pack_int2_fp8(
+        _dev(W8, "W8", torch.uint8, (N, K)), _dev(row_scale, "row_scale", torch.float32, (N,)),
+        N, K, G, _dev(packed, "packed", torch.uint8, (N, K // 4)),
+        _dev(S, "S", torch.bfloat16, (N, K // G)), _dev(ZS, "ZS", torch.bfloat16, (N, K // G)),
+        _stream(stream)))
+    return packed, S, ZS
+
+
+def dh_draft_head_rerank_argmax_fp8(x, W8, row_scale, cand_val, cand_id, rerank, rr_id=None,
+                                    rr_logit=None, argmax_id=None, y_coarse=None,
+                                    workspace=None, stream=None):
+    """dh_draft_head_rerank_argmax against e4m3 rows times their per-row scale."""
+    if W8.dtype == torch.float8_e4m3fn:
+        W8 = W8.view(torch.uint8)
+    x = _bf16(x, "x")
+    M, K = x.shape
+    N = W8.shape[0]
+    ncand = cand_val.shape[1]
+    dev = x.device
+    rr_id = rr_id if rr_id is not None else torch.empty(M, rerank, dtype=torch.int32, device=dev)
+    rr_logit = rr_logit if rr_logit is not None else torch.empty(M, rerank, dtype=torch.float32,
+                                                                  device=dev)
+    argmax_id = argmax_id if argmax_id is not None else torch.empty(M, dtype=torch.int32, device=dev)
+    if workspace is None:
+        raise ValueError("workspace is required (new_workspace)")
+    _check(lib().dh_draft_head_rerank_argmax_fp8(
+        _dev(x, "x", torch.bfloat16), M, K, _dev(W8, "W8", torch.uint8, (N, K)),
+        _dev(row_scale, "row_scale", torch.float32, (N,)), N,
+        _dev(cand_val, "cand_val", torch.float32, (M, ncand)),
+        _dev(cand_id, "cand_id", torch.int32, (M, ncand)), ncand, rerank,
+        _dev(rr_id, "rr_id", torch.int32, (M, rerank)),
+        _dev(rr_logit, "rr_logit", torch.float32, (M, rerank)),
+        _dev(argmax_id, "argmax_id", torch.int32, (M,)),
+        _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    return rr_id, rr_logit, argmax_id
+
+
+def dh_topk_only_logits(rr_id: torch.Tensor, rr_logit: torch.Tensor, N: int, y=None,
+                        stream=None) -> torch.Tensor:
+    """bf16 [M, N] logits for a top-K caller: -inf except the reranked entries (their exact
+    logit rounded to bf16)."""
+    M, R = rr_id.shape
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=rr_id.device)
+    _check(lib().dh_topk_only_logits(_dev(rr_id, "rr_id", torch.int32, (M, R)),
+                                     _dev(rr_logit, "rr_logit", torch.float32, (M, R)), M, R, N,
+                                     _dev(_bf16(y, "y"), "y", torch.bfloat16, (M, N)),
+                                     _stream(stream)))
+    return y
 
 
 def dh_workspace_status(workspace: torch.Tensor, stream=None) -> int:

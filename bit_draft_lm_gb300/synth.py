@@ -173,3 +173,14 @@ def named(name: str) -> Workload:
         M, K, N, seed, big = WORKLOADS[name]
         _CACHE[name] = make_workload(M, K, N, seed, rms_norm=big, lognormal_rows=big, name=name)
     return _CACHE[name]
+
+
+def fp8_head(W: np.ndarray):
+    """An FP8 per-channel head built from a bf16 head (bit patterns uint16 [N, K]): the fp32
+    row scale max|W[n]| / 448 and the e4m3 bytes of W / scale (round to nearest even, the
+    float8_e4m3fn conversion). Returns (W8 uint8 [N, K], scale float32 [N])."""
+    import torch
+    w = torch.from_numpy(np.ascontiguousarray(W).view(np.int16)).view(torch.bfloat16).float()
+    scale = (w.abs().amax(dim=1) / 448.0).clamp(min=1e-12)
+    w8 = (w / scale[:, None]).to(torch.float8_e4m3fn)
+    return w8.view(torch.uint8).numpy().copy(), scale.numpy().astype(np.float32)

@@ -77,6 +77,17 @@ int dh_quantize_pack_int2(const void* W, int64_t N, int64_t K, int G, uint8_t* p
 int dh_quantize_pack_int4(const void* W, int64_t N, int64_t K, int G, uint8_t* packed, void* S,
                           void* ZS, dh_stream_t s);
 
+/*
+ * The int2 quantiser on an FP8 head (_quantize_head_now on _head_matrix's e4m3 rows with their
+ * per-row scale, the compressed-tensors per-channel FP8 lm_head): the values quantised are
+ * fp32(e4m3(W8[n, k])) * row_scale[n] (one fp32 multiply), then exactly as
+ * dh_quantize_pack_int2.
+ *   W8         e4m3 [N, K] row bytes (e4m3 decoded bit-exactly: no NaN handling).   (16-B aligned)
+ *   row_scale  fp32 [N].
+ */
+int dh_quantize_pack_int2_fp8(const uint8_t* W8, const float* row_scale, int64_t N, int64_t K,
+                              int G, uint8_t* packed, void* S, void* ZS, dh_stream_t s);
+
 /* Bytes of packed + S + ZS for one head (0 for unsupported arguments). For N=124160, K=5120,
  * G=128, bits=2 this is 178,790,400 (the page's 0.167 GiB/rank). */
 size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits);
@@ -165,6 +176,28 @@ int dh_draft_head_rerank_argmax_noalloc(const void* x, int64_t M, int64_t K, con
                                         int64_t ncand, int rerank, int32_t* rr_id,
                                         float* rr_logit, int32_t* argmax_id, void* y_coarse,
                                         dh_stream_t s);
+
+/*
+ * dh_draft_head_rerank_argmax against FP8 rows (_rerank_exact with FP8=True): the exact logit is
+ * sum_k x[m, k] * e4m3(W8[n, k]) * row_scale[n], the e4m3 bytes decoded bit-exactly; fp32
+ * accumulation, the row scale applied to the sum. Every other argument and output as there.
+ */
+int dh_draft_head_rerank_argmax_fp8(const void* x, int64_t M, int64_t K, const uint8_t* W8,
+                                    const float* row_scale, int64_t N, const float* cand_val,
+                                    const int32_t* cand_id, int64_t ncand, int rerank,
+                                    int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                                    void* y_coarse, void* workspace, size_t ws_bytes,
+                                    dh_stream_t s);
+
+/*
+ * Logits for a top-K caller (_apply_head_int2 with _radiance_topk_only: y.fill_(-inf) then the
+ * rerank's scatter): y [M, N] bf16 out = -inf everywhere except y[m, rr_id[m, j]] =
+ * bf16(rr_logit[m, j]) (round to nearest even), so that a top-K request draws from exactly the
+ * RERANK reranked entries. rr_id, rr_logit [M, rerank] as written by
+ * dh_draft_head_rerank_argmax; ids outside [0, N) are skipped. Asynchronous on s.
+ */
+int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
+                        int64_t N, void* y, dh_stream_t s);
 
 /*
  * The whole call from and to host memory (_apply_head_int2 end to end): copies x_host (bf16

@@ -17,6 +17,12 @@ patterns. Functions and the passages they follow (page "radiance_drafthead.py"):
 * ``rerank``          -- ``_rerank_exact``: exact logits of the selected rows.
 * ``argmax``          -- the argmax the caller takes.
 * ``exact_logits``    -- brute force over every vocab row.
+* ``topk_only``       -- ``_radiance_topk_only``: ``y.fill_(-inf)`` then the rerank's scatter of
+                         ``ex.to(torch.bfloat16)`` at the reranked ids.
+* ``e4m3_decode``     -- ``_rerank_exact`` (FP8): the exact bit decode of an e4m3 byte.
+* ``quantize_pack_fp8`` -- ``_quantize_head_now`` on an FP8 head (``_head_matrix``): the e4m3
+                         values times the fp32 per-row scale, then the same quantiser.
+* ``rerank_fp8``      -- ``_rerank_exact`` with FP8 rows: sum_k x_k * e4m3(W8[n,k]) * scale[n].
 """
 from __future__ import annotations
 
@@ -54,6 +60,7 @@ def _load():
         I = ctypes.c_int
         sigs = {
             "orc_quantize_pack": [P, I64, I64, I, I, P, P, P, I],
+            "orc_quantize_pack_f32": [P, I64, I64, I, I, P, P, P, I],
             "orc_unpack_codes": [P, I64, I64, I, P],
             "orc_coarse": [P, I64, I64, P, P, P, I64, I, I, P, I],
             "orc_coarse_dequant": [P, I64, I64, P, P, P, I64, I, I, P, I],
@@ -198,3 +205,69 @@ def head(x, packed, S, ZS, W, G=128, bits=2, kcand=8, R=16, nthreads=None):
     am = argmax(e, rr)
     return {"coarse": c, "cand_val": cv, "cand_id": ci, "rr_id": rr, "rr_coarse": rc,
             "rr_logit": e, "argmax": am}
+
+
+def bf16_rne(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def topk_only(rr_id: np.ndarray, rr_logit: np.ndarray, N: int) -> np.ndarray:
+    """bf16 bits [M, N]: -inf (0xFF80) everywhere, then bf16(rr_logit[m, j]) at rr_id[m, j] --
+    the logits a top-K caller ranks (page: ``_radiance_topk_only``)."""
+    M, R = rr_id.shape
+    y = np.full((M, N), 0xFF80, dtype=np.uint16)
+    for m in range(M):
+        for j in range(R):
+            n = int(rr_id[m, j])
+            if 0 <= n < N:
+                y[m, n] = bf16_rne(np.float32(rr_logit[m, j]).reshape(1))[0]
+    return y
+
+
+def e4m3_decode(b: np.ndarray) -> np.ndarray:
+    """e4m3 bytes -> float64, the page's bit decode: exponent e = (b >> 3) & 15, mantissa
+    m = b & 7; e == 0: m * 2^-9, else (1 + m/8) * 2^(e - 7); bit 7 the sign."""
+    b = np.asarray(b, dtype=np.int64)
+    e = (b >> 3) & 15
+    m = (b & 7).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m * 0.125) * np.exp2((e - 7).astype(np.float64)))
+    return np.where((b & 128) != 0, -mag, mag)
+
+
+def quantize_pack_fp8(W8: np.ndarray, scale: np.ndarray, G: int = 128, bits: int = 2,
+                      nthreads: int | None = None):
+    """W8 uint8 [N, K] e4m3 rows, scale fp32 [N] -> (packed, S, ZS) of the values
+    fp32(e4m3(W8)) * fp32(scale) (one IEEE single multiply)."""
+    W8 = np.ascontiguousarray(W8, dtype=np.uint8)
+    N, K = W8.shape
+    Wf = np.ascontiguousarray(e4m3_decode(W8).astype(np.float32) *
+                              np.asarray(scale, dtype=np.float32)[:, None])
+    per = 8 // bits
+    packed = np.empty((N, K // per), dtype=np.uint8)
+    S = np.empty((N, K // G), dtype=np.uint16)
+    ZS = np.empty((N, K // G), dtype=np.uint16)
+    _check(_load().orc_quantize_pack_f32(_p(Wf), N, K, G, bits, _p(packed), _p(S), _p(ZS),
+                                         nthreads or threads()), "quantize_pack_f32")
+    return packed, S, ZS
+
+
+def bf16_bits_to_f64(u: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact)."""
+    return (np.asarray(u, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rerank_fp8(x, W8, scale, ids):
+    """Exact logits against FP8 rows: e[m, j] = sum_k x[m, k] * e4m3(W8[n, k]) * scale[n]
+    (fp64), n = ids[m, j]; -inf for ids outside [0, N)."""
+    xf = bf16_bits_to_f64(np.asarray(x))
+    M, R = ids.shape
+    N = W8.shape[0]
+    e = np.full((M, R), -np.inf)
+    for m in range(M):
+        for j in range(R):
+            n = int(ids[m, j])
+            if 0 <= n < N:
+                e[m, j] = float(np.dot(xf[m], e4m3_decode(W8[n])) * float(scale[n]))
+    return e

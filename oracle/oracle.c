@@ -12,6 +12,7 @@
  *
  * Steps, each following the page:
  *   orc_quantize_pack   asymmetric min/max quantiser, quarter-split (int2) or half-split (int4)
+ *   orc_quantize_pack_f32  the same on fp32 rows (an FP8 head's scaled e4m3 values)
  *                       packing, premultiplied scale S and zero term ZS
  *                       (_quantize_head_now, "Asymmetric min/max at BITS, quarter-split packing").
  *   orc_coarse          c[m,n] = sum_gi ( S*P_gi - ZS*XS_gi ), P_gi = sum_k x_k (1 + v_k/beta),
@@ -106,12 +107,17 @@ static void parallel_for(int64_t n, int nthreads, range_fn fn, void* ctx) {
  * Packing, int4 (H = K/2): byte j = q[j] | q[H+j] << 4.
  */
 typedef struct {
-  const uint16_t* W;
+  const uint16_t* W; /* bf16 rows, or */
+  const float* Wf;   /* fp32 rows (an FP8 head's e4m3 values times the row scale) */
   int64_t K;
   int G, bits;
   uint8_t* packed;
   uint16_t *S, *ZS;
 } quant_ctx;
+
+static float wval(const quant_ctx* c, int64_t n, int64_t k) {
+  return c->Wf ? c->Wf[n * c->K + k] : bf16_to_float(c->W[n * c->K + k]);
+}
 
 static void quant_rows(void* p, int64_t lo_row, int64_t hi_row) {
   quant_ctx* c = (quant_ctx*)p;
@@ -123,11 +129,10 @@ static void quant_rows(void* p, int64_t lo_row, int64_t hi_row) {
   uint8_t* q = (uint8_t*)malloc((size_t)K);
   if (!q) return;
   for (int64_t n = lo_row; n < hi_row; ++n) {
-    const uint16_t* w = c->W + n * K;
     for (int64_t gi = 0; gi < ng; ++gi) {
-      float lo = bf16_to_float(w[gi * G]), hi = lo;
+      float lo = wval(c, n, gi * G), hi = lo;
       for (int t = 1; t < G; ++t) {
-        float v = bf16_to_float(w[gi * G + t]);
+        float v = wval(c, n, gi * G + t);
         if (v < lo) lo = v;
         if (v > hi) hi = v;
       }
@@ -137,7 +142,7 @@ static void quant_rows(void* p, int64_t lo_row, int64_t hi_row) {
       if (zp < 0.0f) zp = 0.0f;
       if (zp > lv) zp = lv;
       for (int t = 0; t < G; ++t) {
-        float v = bf16_to_float(w[gi * G + t]);
+        float v = wval(c, n, gi * G + t);
         float r = rintf(v / sc + zp);
         if (r < 0.0f) r = 0.0f;
         if (r > lv) r = lv;
@@ -168,7 +173,21 @@ int orc_quantize_pack(const uint16_t* W, int64_t N, int64_t K, int G, int bits, 
   if (N <= 0 || K <= 0 || G <= 0 || (bits != 2 && bits != 4)) return -2;
   if (K % G) return -2;
   if (K % (8 / bits)) return -2;
-  quant_ctx c = {W, K, G, bits, packed, S, ZS};
+  quant_ctx c = {W, NULL, K, G, bits, packed, S, ZS};
+  parallel_for(N, nthreads, quant_rows, &c);
+  return 0;
+}
+
+/* The same quantiser on fp32 rows: an FP8 head's values e4m3(b) * row_scale (page
+ * _quantize_head_now: `wg = w.data[i:j].to(torch.float32) * wsc[i:j, None]`, one fp32 multiply,
+ * done by the caller). */
+int orc_quantize_pack_f32(const float* Wf, int64_t N, int64_t K, int G, int bits,
+                          uint8_t* packed, uint16_t* S, uint16_t* ZS, int nthreads) {
+  if (!Wf || !packed || !S || !ZS) return -1;
+  if (N <= 0 || K <= 0 || G <= 0 || (bits != 2 && bits != 4)) return -2;
+  if (K % G) return -2;
+  if (K % (8 / bits)) return -2;
+  quant_ctx c = {NULL, Wf, K, G, bits, packed, S, ZS};
   parallel_for(N, nthreads, quant_rows, &c);
   return 0;
 }

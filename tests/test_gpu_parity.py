@@ -339,3 +339,59 @@ def test_draft_head_host_entry_point():
         gam, grr, grl = head.infer(x_host)
         assert torch.equal(am, gam) and torch.equal(rr, grr) and torch.equal(rl, grl)
     assert dh.dh_workspace_status(head.workspace) == 0
+
+
+@pytest.mark.parametrize("M,K,N,seed", [(1, 1024, 8192, 44), (3, 1024, 8232, 45)])
+def test_topk_only_logits(M, K, N, seed):
+    """dh_topk_only_logits after the full path: bit-exact against the oracle's construction from
+    the same reranked ids and logits (every other entry -inf)."""
+    w = synth.make_workload(M, K, N, seed, plant=True)
+    W, packed, S, ZS = _gpu_quant(w.W, 128, 2)
+    x = dev_bf16(w.x)
+    ws = dh.new_workspace(M, N, K, 8, 16)
+    cv, ci = dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, 128, 2, 8, workspace=ws)
+    rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, 16, workspace=ws)
+    y = dh.dh_topk_only_logits(rr, rl, N)
+    torch.cuda.synchronize()
+    expect = oracle.topk_only(rr.cpu().numpy(), rl.cpu().numpy(), N)
+    assert np.array_equal(host_u16(y), expect)
+
+
+FP8_CASES = [
+    # M, K, N, R, seed
+    (1, 1024, 8192, 16, 50),   # the cluster rerank
+    (4, 2048, 20000, 16, 51),
+    (3, 1024, 8232, 48, 52),   # R > 32: the one-CTA rerank
+]
+
+
+@pytest.mark.parametrize("M,K,N,R,seed", FP8_CASES)
+def test_fp8_head_parity(M, K, N, R, seed):
+    """FP8 head (e4m3 rows + fp32 per-row scale): the int2 quantiser on the scaled e4m3 values
+    bit-exact against the oracle; the FP8 rerank's logits within the rerank tolerance of the
+    oracle's fp64 values on the selected ids, and its argmax equal on every row that is not a
+    near tie."""
+    w = synth.make_workload(M, K, N, seed, plant=True)
+    W8h, sc = synth.fp8_head(w.W)
+    W8, scd = torch.from_numpy(W8h).cuda(), torch.from_numpy(sc).cuda()
+    packed, S, ZS = dh.dh_quantize_pack_int2_fp8(W8, scd, 128)
+    op, oS, oZS = oracle.quantize_pack_fp8(W8h, sc, 128)
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), op)
+    assert np.array_equal(host_u16(S), oS) and np.array_equal(host_u16(ZS), oZS)
+    x = dev_bf16(w.x)
+    ws = dh.new_workspace(M, N, K, 8, R)
+    cv, ci = dh.dh_draft_head_coarse_topk(x, packed, S, ZS, N, 128, 2, 8, workspace=ws)
+    rr, rl, am = dh.dh_draft_head_rerank_argmax_fp8(x, W8, scd, cv, ci, R, workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.dh_workspace_status(ws) == 0
+    g_rr = rr.cpu().numpy()
+    e = oracle.rerank_fp8(w.x, W8h, sc, g_rr)
+    gl = rl.cpu().numpy().astype(np.float64)
+    xf = bf16_to_f64(w.x)
+    wf = oracle.e4m3_decode(W8h) * sc.astype(np.float64)[:, None]
+    mag = np.stack([np.abs(xf[m][None, :] * wf[g_rr[m]]).sum(axis=1) for m in range(M)])
+    assert np.all(np.abs(gl - e) <= 1e-4 * np.abs(e) + 1e-6 * mag)
+    o_am = oracle.argmax(e, g_rr)
+    ok = ~near_tie_rows(e)
+    assert np.array_equal(am.cpu().numpy()[ok], o_am[ok])

@@ -298,3 +298,66 @@ def test_unreranked_coarse_is_not_exact():
     c = oracle.coarse(w.x, packed, S, ZS)
     ex = oracle.exact_logits(w.x, w.W)
     assert int(np.argmax(c[0])) != int(np.argmax(ex[0]))
+
+
+def test_topk_only_oracle():
+    """topk_only (the page's y.fill_(-inf) + scatter of bf16 exact logits): bf16 rounding is
+    round-to-nearest-even (checked against torch's own conversion, an independent
+    implementation, and on hand-picked ties); every entry but the R reranked ones is -inf."""
+    import torch
+    v = np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -2.5, 3.0e-3, -7.123e4],
+                 dtype=np.float32)
+    got = oracle.bf16_rne(v)
+    assert got[0] == 0x3F80 and got[1] == 0x3F80 and got[2] == 0x3F82 and got[3] == 0xC020
+    rng = np.random.default_rng(7)
+    r = (rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 6, 4096)).astype(np.float32)
+    ref = torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_rne(r), ref)
+    M, R, N = 3, 16, 1000
+    ids = np.stack([rng.choice(N, R, replace=False) for _ in range(M)]).astype(np.int32)
+    lg = rng.standard_normal((M, R)).astype(np.float32)
+    y = oracle.topk_only(ids, lg, N)
+    assert y.shape == (M, N)
+    for m in range(M):
+        fin = np.flatnonzero(y[m] != 0xFF80)
+        assert np.array_equal(np.sort(fin), np.sort(ids[m]))
+        assert np.array_equal(y[m, ids[m]], oracle.bf16_rne(lg[m]))
+
+
+def test_e4m3_decode_matches_torch():
+    """The page's e4m3 bit decode (oracle) equals torch's float8_e4m3fn conversion (an
+    independent implementation) on every byte that is not a NaN."""
+    import torch
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    dec = oracle.e4m3_decode(b)
+    ok = ~np.isnan(ref)
+    assert ok.sum() == 254
+    assert np.array_equal(dec[ok], ref[ok])
+
+
+def test_fp8_quantiser_and_rerank_pins():
+    """FP8 head: with a row scale of 1, quantising the scaled e4m3 values (fp32 rows) gives the
+    same bytes as quantising the same values stored as bf16 (every e4m3 value is a bf16 value),
+    so the fp32 path is pinned to the bf16 quantiser; a power-of-two row scale scales S and ZS
+    exactly and leaves the codes; the FP8 rerank of a one-hot x is e4m3(w) * scale exactly."""
+    rng = np.random.default_rng(11)
+    N, K, G = 6, 512, 128
+    W8 = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    W8[(W8 & 0x7F) == 0x7F] = 0x3C  # no NaN bytes
+    one = np.ones(N, dtype=np.float32)
+    p8, S8, Z8 = oracle.quantize_pack_fp8(W8, one, G)
+    Wb = oracle.bf16_rne(oracle.e4m3_decode(W8).astype(np.float32))
+    pb, Sb, Zb = oracle.quantize_pack(Wb, G, 2)
+    assert np.array_equal(p8, pb) and np.array_equal(S8, Sb) and np.array_equal(Z8, Zb)
+    p4, S4, Z4 = oracle.quantize_pack_fp8(W8, one * 0.25, G)
+    assert np.array_equal(p4, p8)
+    assert np.array_equal(oracle.bf16_bits_to_f64(S4), oracle.bf16_bits_to_f64(S8) * 0.25)
+    assert np.array_equal(oracle.bf16_bits_to_f64(Z4), oracle.bf16_bits_to_f64(Z8) * 0.25)
+    scale = rng.uniform(0.001, 0.01, N).astype(np.float32)
+    k = 77
+    x = np.zeros((1, K), dtype=np.uint16)
+    x[0, k] = 0x3F80  # 1.0
+    ids = np.arange(N, dtype=np.int32)[None, :]
+    e = oracle.rerank_fp8(x, W8, scale, ids)
+    assert np.array_equal(e[0], oracle.e4m3_decode(W8[:, k]) * scale.astype(np.float64))
