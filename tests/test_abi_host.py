@@ -120,3 +120,54 @@ def test_status_validation(lib):
 def test_last_error_cleared_by_success_path_message(lib):
     _coarse(lib, G=7)
     assert "G=7" in dh.dh_last_error()
+
+
+def test_workspace_bytes_sizes(lib):
+    """Up to 16 hidden rows the workspace is the 256-byte header; beyond, the tensor-core pass
+    keeps its scratch after it: x as the MMA operand (80 x K x 2 B), group sums (80 x K/64 x 4 B)
+    and exponents (80 x 4 B), each rounded up to 256 B."""
+    assert dh.dh_workspace_bytes(1, 124160, 5120, 8, 16) == 256
+    assert dh.dh_workspace_bytes(16, 124160, 5120, 8, 16) == 256
+    r = lambda v: (v + 255) // 256 * 256
+    assert dh.dh_workspace_bytes(72, 124160, 5120, 8, 16) == \
+        256 + r(80 * 5120 * 2) + r(80 * 80 * 4) + r(80 * 4)
+    assert dh.dh_workspace_bytes(0, 124160, 5120, 8, 16) == 0
+
+
+def test_fp8_and_topk_validation(lib):
+    f = lib.dh_quantize_pack_int2_fp8
+    assert f(A16, None, 64, 1024, 128, A16, A16, A16, None) == dh.DH_ERR_NULL
+    assert f(None, A16, 64, 1024, 128, A16, A16, A16, None) == dh.DH_ERR_NULL
+    assert f(A16, A16, 64, 1000, 128, A16, A16, A16, None) == dh.DH_ERR_SHAPE
+    assert f(A16, A16 + 2, 64, 1024, 128, A16, A16, A16, None) == dh.DH_ERR_ALIGN
+    g = lib.dh_draft_head_rerank_argmax_fp8
+    args = [A16, 1, 1024, A16, A16, 8192, A16, A16, 1024, 16, A16, A16, A16, None, A256, 256, None]
+    bad = list(args); bad[3] = None
+    assert g(*bad) == dh.DH_ERR_NULL
+    bad = list(args); bad[4] = None
+    assert g(*bad) == dh.DH_ERR_NULL
+    bad = list(args); bad[9] = 0
+    assert g(*bad) == dh.DH_ERR_PARAM
+    bad = list(args); bad[3] = A16 + 8
+    assert g(*bad) == dh.DH_ERR_ALIGN
+    t = lib.dh_topk_only_logits
+    assert t(None, A16, 1, 16, 8192, A16, None) == dh.DH_ERR_NULL
+    assert t(A16, A16, 0, 16, 8192, A16, None) == dh.DH_ERR_SHAPE
+    assert t(A16, A16, 1, 0, 8192, A16, None) == dh.DH_ERR_SHAPE
+    assert t(A16 + 2, A16, 1, 16, 8192, A16, None) == dh.DH_ERR_ALIGN
+
+
+def test_host_call_validation(lib):
+    h = lib.dh_draft_head_host
+    args = [A16, 1, 1024, A16, A16, A16, A16, A16, 8192, 128, 2, 8, 16, A16, A16, A16, A16, A16,
+            A16, A16, A16, A256, 256, None]
+    bad = list(args); bad[0] = None
+    assert h(*bad) == dh.DH_ERR_NULL
+    bad = list(args); bad[18] = None
+    assert h(*bad) == dh.DH_ERR_NULL
+    bad = list(args); bad[1] = 0
+    assert h(*bad) == dh.DH_ERR_SHAPE
+    bad = list(args); bad[12] = 300
+    assert h(*bad) == dh.DH_ERR_SHAPE
+    bad = list(args); bad[3] = A16 + 4
+    assert h(*bad) == dh.DH_ERR_ALIGN
