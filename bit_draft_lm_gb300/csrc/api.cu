@@ -149,12 +149,10 @@ int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
 size_t rerank_workspace_needed() { return rerank_workspace_bytes(); }
 }  // namespace dh
 
-static int rerank_impl(const char* who, const void* x, int64_t M, int64_t K, const void* W,
-                       const uint8_t* W8, const float* wscale, int64_t N,
-                                const float* cand_val, const int32_t* cand_id, int64_t ncand,
-                                int rerank, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
-                                void* y_coarse, void* workspace, size_t ws_bytes,
-                                dh_stream_t s) {
+static int check_rerank(const char* who, const void* x, int64_t M, int64_t K, const void* W,
+                        const uint8_t* W8, const float* wscale, int64_t N, const float* cand_val,
+                        const int32_t* cand_id, int64_t ncand, int rerank, int32_t* rr_id,
+                        float* rr_logit, int32_t* argmax_id, void* y_coarse) {
   if (!x || (!W && !W8) || (W8 && !wscale) || !cand_val || !cand_id || !rr_id || !rr_logit || !argmax_id)
     return fail(DH_ERR_NULL, "%s: NULL pointer", who);
   if (rerank < 1 || rerank > DH_MAX_RERANK)
@@ -171,7 +169,18 @@ static int rerank_impl(const char* who, const void* x, int64_t M, int64_t K, con
   if (!aligned(cand_val, 4) || !aligned(cand_id, 4) || !aligned(rr_id, 4) ||
       !aligned(rr_logit, 4) || !aligned(argmax_id, 4) || (y_coarse && !aligned(y_coarse, 2)))
     return fail(DH_ERR_ALIGN, "%s: misaligned candidate or output array", who);
-  int rc = check_workspace(workspace, ws_bytes, rerank_workspace_bytes(), who);
+  return DH_OK;
+}
+
+static int rerank_impl(const char* who, const void* x, int64_t M, int64_t K, const void* W,
+                       const uint8_t* W8, const float* wscale, int64_t N, const float* cand_val,
+                       const int32_t* cand_id, int64_t ncand, int rerank, int32_t* rr_id,
+                       float* rr_logit, int32_t* argmax_id, void* y_coarse, void* workspace,
+                       size_t ws_bytes, dh_stream_t s) {
+  int rc = check_rerank(who, x, M, K, W, W8, wscale, N, cand_val, cand_id, ncand, rerank, rr_id,
+                        rr_logit, argmax_id, y_coarse);
+  if (rc != DH_OK) return rc;
+  rc = check_workspace(workspace, ws_bytes, rerank_workspace_bytes(), who);
   if (rc != DH_OK) return rc;
   dh::RerankCall r{x, M, K, W, N, cand_val, cand_id, ncand, rerank, rr_id, rr_logit, argmax_id,
                    y_coarse, static_cast<uint32_t*>(workspace), W8, wscale};
@@ -223,11 +232,11 @@ size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank
   return c > r ? c : r;
 }
 
-int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
-                              const void* S, const void* ZS, int64_t N, int G, int bits,
-                              int kcand, float* cand_val, int32_t* cand_id, void* y_coarse,
-                              void* workspace, size_t ws_bytes, dh_stream_t s) {
-  const char* who = "draft_head_coarse_topk";
+}  // extern "C"
+
+static int check_coarse(const char* who, const void* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const void* S, const void* ZS, int64_t N, int G,
+                        int bits, int kcand, float* cand_val, int32_t* cand_id, void* y_coarse) {
   if (!x || !packed || !S || !ZS || !cand_val || !cand_id)
     return fail(DH_ERR_NULL, "%s: NULL pointer", who);
   if (bits != 2 && bits != 4) return fail(DH_ERR_PARAM, "%s: bits=%d (2 or 4)", who, bits);
@@ -248,7 +257,20 @@ int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t
     return fail(DH_ERR_ALIGN, "%s: x, packed, S and ZS must be 16-byte aligned", who);
   if (!aligned(cand_val, 4) || !aligned(cand_id, 4) || (y_coarse && !aligned(y_coarse, 2)))
     return fail(DH_ERR_ALIGN, "%s: output misaligned", who);
-  int rc = check_workspace(workspace, ws_bytes, coarse_workspace_bytes(M, K), who);
+  return DH_OK;
+}
+
+extern "C" {
+
+int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                              const void* S, const void* ZS, int64_t N, int G, int bits,
+                              int kcand, float* cand_val, int32_t* cand_id, void* y_coarse,
+                              void* workspace, size_t ws_bytes, dh_stream_t s) {
+  const char* who = "draft_head_coarse_topk";
+  int rc = check_coarse(who, x, M, K, packed, S, ZS, N, G, bits, kcand, cand_val, cand_id,
+                        y_coarse);
+  if (rc != DH_OK) return rc;
+  rc = check_workspace(workspace, ws_bytes, coarse_workspace_bytes(M, K), who);
   if (rc != DH_OK) return rc;
   DeviceInfo di;
   cudaError_t e = device_info(di);
@@ -287,6 +309,47 @@ int dh_draft_head_rerank_argmax_fp8(const void* x, int64_t M, int64_t K, const u
   return rerank_impl("draft_head_rerank_argmax_fp8", x, M, K, nullptr, W8, row_scale, N,
                      cand_val, cand_id, ncand, rerank, rr_id, rr_logit, argmax_id, y_coarse,
                      workspace, ws_bytes, s);
+}
+
+int dh_draft_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                         const void* S, const void* ZS, const void* W, int64_t N, int G, int bits,
+                         int kcand, int rerank, float* cand_val, int32_t* cand_id, int32_t* rr_id,
+                         float* rr_logit, int32_t* argmax_id, void* y_coarse, void* workspace,
+                         size_t ws_bytes, dh_stream_t s) {
+  const char* who = "draft_head_argmax";
+  int rc = check_coarse(who, x, M, K, packed, S, ZS, N, G, bits, kcand, cand_val, cand_id,
+                        y_coarse);
+  if (rc != DH_OK) return rc;
+  if (!W) return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  const int64_t ncand = ((N + DH_BLOCK_ROWS - 1) / DH_BLOCK_ROWS) * kcand;
+  rc = check_rerank(who, x, M, K, W, nullptr, nullptr, N, cand_val, cand_id, ncand, rerank, rr_id,
+                    rr_logit, argmax_id, y_coarse);
+  if (rc != DH_OK) return rc;
+  rc = check_workspace(workspace, ws_bytes, dh_workspace_bytes(M, N, K, kcand, rerank), who);
+  if (rc != DH_OK) return rc;
+  DeviceInfo di;
+  cudaError_t e = device_info(di);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  void* scratch = dh::coarse_wide_scratch_bytes(M, K)
+                      ? static_cast<unsigned char*>(workspace) + kWorkspaceHeader
+                      : nullptr;
+  uint32_t* status = static_cast<uint32_t*>(workspace);
+  dh::CoarseCall cc{x,        M,       K,        packed, S,  ZS, N, G, bits, kcand,
+                    cand_val, cand_id, y_coarse, status, scratch};
+  e = dh::launch_coarse_topk(cc, di.sms, di.max_smem, cs);
+  if (e == cudaErrorInvalidValue)
+    return fail(DH_ERR_SHAPE, "%s: shape does not fit the kernel's shared-memory plan", who);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_argmax coarse launch");
+  // the rerank's cluster kernel starts as a programmatic dependent of the coarse pass: it stages
+  // x while the coarse pass finishes and waits for the candidates
+  dh::RerankCall r{x,       M,     K,      W,     N,        cand_val,  cand_id,
+                   ncand,   rerank, rr_id, rr_logit, argmax_id, y_coarse, status};
+  e = dh::launch_rerank_argmax(r, cs);
+  if (e == cudaErrorInvalidValue)
+    return fail(DH_ERR_SHAPE, "%s: candidate count does not fit the rerank kernel", who);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_argmax rerank launch");
+  return ok();
 }
 
 int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
@@ -362,18 +425,13 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
     e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: begin capture");
     const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
-    const int64_t ncand = ((N + DH_BLOCK_ROWS - 1) / DH_BLOCK_ROWS) * kcand;
     const size_t rb = static_cast<size_t>(M) * static_cast<size_t>(rerank) * 4;
     int rc = DH_OK;
     e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) {
-      rc = dh_draft_head_coarse_topk(x_dev, M, K, packed, S, ZS, N, G, bits, kcand, cand_val,
-                                     cand_id, nullptr, workspace, ws_bytes,
-                                     reinterpret_cast<dh_stream_t>(cs));
-      if (rc == DH_OK)
-        rc = dh_draft_head_rerank_argmax(x_dev, M, K, W, N, cand_val, cand_id, ncand, rerank,
-                                         rr_id, rr_logit, argmax_id, nullptr, workspace,
-                                         ws_bytes, reinterpret_cast<dh_stream_t>(cs));
+      rc = dh_draft_head_argmax(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank,
+                                cand_val, cand_id, rr_id, rr_logit, argmax_id, nullptr,
+                                workspace, ws_bytes, reinterpret_cast<dh_stream_t>(cs));
       if (rc == DH_OK) {
         // one copy when the three results lie back to back on both sides (argmax, rr_id,
         // rr_logit), else three

@@ -43,6 +43,8 @@ SIGNATURES = {
                                    _SZ, _P], _I),
     "dh_draft_head_rerank_argmax": ([_P, _I64, _I64, _P, _I64, _P, _P, _I64, _I, _P, _P, _P, _P,
                                      _P, _SZ, _P], _I),
+    "dh_draft_head_argmax": ([_P, _I64, _I64, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
+                              _P, _P, _P, _P, _SZ, _P], _I),
     "dh_draft_head_rerank_argmax_noalloc": ([_P, _I64, _I64, _P, _I64, _P, _P, _I64, _I, _P,
                                              _P, _P, _P, _P], _I),
     "dh_draft_head_host": ([_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
@@ -221,6 +223,48 @@ def dh_draft_head_rerank_argmax(x: torch.Tensor, W: torch.Tensor, cand_val: torc
     return rr_id, rr_logit, argmax_id
 
 
+def dh_draft_head_argmax(x: torch.Tensor, packed: torch.Tensor, S: torch.Tensor,
+                         ZS: torch.Tensor, W: torch.Tensor, G: int = 128, bits: int = 2,
+                         kcand: int = 8, rerank: int = 16, cand_val=None, cand_id=None,
+                         rr_id=None, rr_logit=None, argmax_id=None, y_coarse=None,
+                         workspace=None, stream=None):
+    """Coarse pass, global top-R, exact rerank and argmax in one call (the coarse and rerank
+    kernels, validated together). -> (rr_id i32 [M, R], rr_logit f32 [M, R], argmax_id i32 [M],
+    cand_val, cand_id)."""
+    x = _bf16(x, "x")
+    W = _bf16(W, "W")
+    M, K = x.shape
+    N = W.shape[0]
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    dev = x.device
+    if cand_val is None:
+        cand_val = torch.empty(M, nblk * kcand, dtype=torch.float32, device=dev)
+    if cand_id is None:
+        cand_id = torch.empty(M, nblk * kcand, dtype=torch.int32, device=dev)
+    if rr_id is None:
+        rr_id = torch.empty(M, rerank, dtype=torch.int32, device=dev)
+    if rr_logit is None:
+        rr_logit = torch.empty(M, rerank, dtype=torch.float32, device=dev)
+    if argmax_id is None:
+        argmax_id = torch.empty(M, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(M, N, K, kcand, rerank, dev)
+    if y_coarse is not None:
+        y_coarse = _bf16(y_coarse, "y_coarse")
+    _check(lib().dh_draft_head_argmax(
+        _dev(x, "x", torch.bfloat16), M, K, _dev(packed, "packed", torch.uint8),
+        _dev(_bf16(S, "S"), "S", torch.bfloat16), _dev(_bf16(ZS, "ZS"), "ZS", torch.bfloat16),
+        _dev(W, "W", torch.bfloat16, (N, K)), N, G, bits, kcand, rerank,
+        _dev(cand_val, "cand_val", torch.float32, (M, nblk * kcand)),
+        _dev(cand_id, "cand_id", torch.int32, (M, nblk * kcand)),
+        _dev(rr_id, "rr_id", torch.int32, (M, rerank)),
+        _dev(rr_logit, "rr_logit", torch.float32, (M, rerank)),
+        _dev(argmax_id, "argmax_id", torch.int32, (M,)),
+        _dev(y_coarse, "y_coarse", torch.bfloat16, (M, N)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    return rr_id, rr_logit, argmax_id, cand_val, cand_id
+
+
 def dh_draft_head_rerank_argmax_noalloc(x: torch.Tensor, W: torch.Tensor,
                                         cand_val: torch.Tensor, cand_id: torch.Tensor,
                                         rerank: int = 16, rr_id=None, rr_logit=None,
@@ -359,8 +403,9 @@ class DraftHead:
         with the same M overwrites).
 
         The step is one CUDA graph per M, captured on the first call: the copy in (from a
-        pinned staging buffer that x_host is copied into on the host), the coarse pass, the
-        rerank and one copy out of the three results, which sit in one device buffer."""
+        pinned staging buffer that x_host is copied into on the host), dh_draft_head_argmax
+        (the coarse and rerank kernels) and one copy out of the three results, which sit in one
+        device buffer."""
         M = x_host.shape[0]
         if M < 1 or M > self.max_tokens:
             raise ValueError(f"M={M} outside 1..max_tokens={self.max_tokens}")
@@ -428,12 +473,10 @@ class DraftHead:
 
         def step():
             g["d_x"].copy_(g["h_x"], non_blocking=True)
-            cv, ci = dh_draft_head_coarse_topk(g["d_x"], self.packed, self.S, self.ZS, self.N,
-                                               self.G, self.bits, self.kcand,
-                                               cand_val=self._cv[:M], cand_id=self._ci[:M],
-                                               workspace=self.workspace)
-            dh_draft_head_rerank_argmax(g["d_x"], self.W, cv, ci, R, rr_id=d_rr, rr_logit=d_rl,
-                                        argmax_id=d_am, workspace=self.workspace)
+            dh_draft_head_argmax(g["d_x"], self.packed, self.S, self.ZS, self.W, self.G,
+                                 self.bits, self.kcand, R, cand_val=self._cv[:M],
+                                 cand_id=self._ci[:M], rr_id=d_rr, rr_logit=d_rl,
+                                 argmax_id=d_am, workspace=self.workspace)
             g["h_out"].copy_(g["d_out"], non_blocking=True)
 
         side = torch.cuda.Stream()
@@ -456,12 +499,9 @@ class DraftHead:
         if x.shape[0] > self.max_tokens:
             raise ValueError(f"M={x.shape[0]} > max_tokens={self.max_tokens}")
         M = x.shape[0]
-        cv, ci = dh_draft_head_coarse_topk(x, self.packed, self.S, self.ZS, self.N, self.G,
-                                           self.bits, self.kcand, cand_val=self._cv[:M],
-                                           cand_id=self._ci[:M], y_coarse=y_coarse,
-                                           workspace=self.workspace, stream=stream)
-        rr, rl, am = dh_draft_head_rerank_argmax(x, self.W, cv, ci, self.rerank,
-                                                 rr_id=self._rr[:M], rr_logit=self._rl[:M],
-                                                 argmax_id=self._am[:M], y_coarse=y_coarse,
-                                                 workspace=self.workspace, stream=stream)
+        rr, rl, am, cv, ci = dh_draft_head_argmax(
+            x, self.packed, self.S, self.ZS, self.W, self.G, self.bits, self.kcand, self.rerank,
+            cand_val=self._cv[:M], cand_id=self._ci[:M], rr_id=self._rr[:M],
+            rr_logit=self._rl[:M], argmax_id=self._am[:M], y_coarse=y_coarse,
+            workspace=self.workspace, stream=stream)
         return {"argmax": am, "rr_id": rr, "rr_logit": rl, "cand_val": cv, "cand_id": ci}

@@ -92,9 +92,9 @@ int dh_quantize_pack_int2_fp8(const uint8_t* W8, const float* row_scale, int64_t
  * G=128, bits=2 this is 178,790,400 (the page's 0.167 GiB/rank). */
 size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits);
 
-/* Workspace bytes the two per-call entry points need for these sizes (one workspace serves
- * both). The workspace must be zero-filled once before first use; calls sharing a workspace
- * must be ordered on one stream. The rerank needs the 256-byte header (status word) only; the
+/* Workspace bytes the per-call entry points need for these sizes (one workspace serves them
+ * all). The workspace must be zero-filled once before first use; calls sharing a workspace
+ * must be ordered on one stream. The rerank needs the 256-byte header (status word) only. The
  * coarse pass of more than 16 hidden rows of an int2 head (its tensor-core path) also keeps its
  * scratch after the header: the hidden states laid out as the MMA operand (80 * K * 2 bytes),
  * their group sums and scales. */
@@ -149,6 +149,22 @@ int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void*
                                 void* y_coarse, void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
+ * The whole device-side call (the page's _apply_head_int2 from hidden states to the argmax):
+ * dh_draft_head_coarse_topk followed by dh_draft_head_rerank_argmax on the same stream, with
+ * the arguments and outputs of the two calls (ncand = ceil(N/64) * kcand; y_coarse, when given,
+ * holds the coarse logits with the reranked entries scattered over them) and bit-identical
+ * results. The arguments of both are validated before anything is launched, and the rerank's
+ * kernel starts as a programmatic dependent of the coarse pass.
+ *   workspace: ws_bytes >= dh_workspace_bytes(M, N, K, kcand, rerank), zero-filled before its
+ *   first use.
+ */
+int dh_draft_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                         const void* S, const void* ZS, const void* W, int64_t N, int G, int bits,
+                         int kcand, int rerank, float* cand_val, int32_t* cand_id, int32_t* rr_id,
+                         float* rr_logit, int32_t* argmax_id, void* y_coarse, void* workspace,
+                         size_t ws_bytes, dh_stream_t s);
+
+/*
  * Rerank + argmax without a caller workspace. The page has no counterpart to this entry point:
  * it is for callers that cannot allocate device memory -- a plug-in handed only its input and
  * output buffers, code running inside another framework's memory pool or allocator, or a
@@ -201,12 +217,12 @@ int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, 
 
 /*
  * The whole call from and to host memory (_apply_head_int2 end to end): copies x_host (bf16
- * [M, K]) into x_dev, runs dh_draft_head_coarse_topk and dh_draft_head_rerank_argmax, copies
+ * [M, K]) into x_dev, runs dh_draft_head_argmax, copies
  * argmax [M], rr_id [M, rerank] and rr_logit [M, rerank] back into argmax_host, rr_id_host and
  * rr_logit_host, and synchronises (the one call besides dh_workspace_status that does).
  * x_host and the three host arrays must be page-locked (pinned) memory.
- *   x_dev, cand_val, cand_id, rr_id, rr_logit, argmax_id, workspace: device buffers as for the
- *   two calls it makes (their device outputs are written too); the other arguments likewise.
+ *   x_dev, cand_val, cand_id, rr_id, rr_logit, argmax_id, workspace: device buffers as for
+ *   dh_draft_head_argmax (its device outputs are written too); the other arguments likewise.
  * The sequence is captured into a CUDA graph the first time an argument set is seen on a
  * device (on a stream of the library's own) and replayed on s on later calls. The library
  * keeps the 16 most recent such graphs and one capture stream per device, no device memory. Returns DH_ERR_PARAM while s is being captured; otherwise the first failing step's

@@ -171,3 +171,23 @@ def test_host_call_validation(lib):
     assert h(*bad) == dh.DH_ERR_SHAPE
     bad = list(args); bad[3] = A16 + 4
     assert h(*bad) == dh.DH_ERR_ALIGN
+
+
+def test_argmax_call_validation(lib):
+    """dh_draft_head_argmax rejects bad arguments before anything is launched (every case here
+    fails validation: the addresses are not real device memory)."""
+    f = lib.dh_draft_head_argmax
+    args = [A16, 1, 1024, A16, A16, A16, A16, 8192, 128, 2, 8, 16, A16, A16, A16, A16, A16, None,
+            A256, 256, None]
+    bad = list(args); bad[6] = None      # W
+    assert f(*bad) == dh.DH_ERR_NULL
+    bad = list(args); bad[3] = None      # packed
+    assert f(*bad) == dh.DH_ERR_NULL
+    bad = list(args); bad[11] = 0        # rerank
+    assert f(*bad) == dh.DH_ERR_PARAM
+    bad = list(args); bad[9] = 3         # bits
+    assert f(*bad) == dh.DH_ERR_PARAM
+    bad = list(args); bad[6] = A16 + 2   # W misaligned
+    assert f(*bad) == dh.DH_ERR_ALIGN
+    bad = list(args); bad[19] = 128      # smaller than the 256-byte header
+    assert f(*bad) == dh.DH_ERR_WORKSPACE
