@@ -311,11 +311,16 @@ int dh_draft_head_rerank_argmax_fp8(const void* x, int64_t M, int64_t K, const u
                      workspace, ws_bytes, s);
 }
 
-int dh_draft_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* packed,
-                         const void* S, const void* ZS, const void* W, int64_t N, int G, int bits,
-                         int kcand, int rerank, float* cand_val, int32_t* cand_id, int32_t* rr_id,
-                         float* rr_logit, int32_t* argmax_id, void* y_coarse, void* workspace,
-                         size_t ws_bytes, dh_stream_t s) {
+}  // extern "C"
+
+// dh_draft_head_argmax, optionally also writing the three results into page-locked host arrays
+// through their device views (h_*: all three or none).
+static int argmax_impl(const void* x, int64_t M, int64_t K, const uint8_t* packed, const void* S,
+                       const void* ZS, const void* W, int64_t N, int G, int bits, int kcand,
+                       int rerank, float* cand_val, int32_t* cand_id, int32_t* rr_id,
+                       float* rr_logit, int32_t* argmax_id, void* y_coarse, void* workspace,
+                       size_t ws_bytes, dh_stream_t s, int32_t* h_argmax_id = nullptr,
+                       int32_t* h_rr_id = nullptr, float* h_rr_logit = nullptr) {
   const char* who = "draft_head_argmax";
   int rc = check_coarse(who, x, M, K, packed, S, ZS, N, G, bits, kcand, cand_val, cand_id,
                         y_coarse);
@@ -345,11 +350,25 @@ int dh_draft_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* pac
   // x while the coarse pass finishes and waits for the candidates
   dh::RerankCall r{x,       M,     K,      W,     N,        cand_val,  cand_id,
                    ncand,   rerank, rr_id, rr_logit, argmax_id, y_coarse, status};
+  r.h_rr_id = h_rr_id;
+  r.h_rr_logit = h_rr_logit;
+  r.h_argmax_id = h_argmax_id;
   e = dh::launch_rerank_argmax(r, cs);
   if (e == cudaErrorInvalidValue)
     return fail(DH_ERR_SHAPE, "%s: candidate count does not fit the rerank kernel", who);
   if (e != cudaSuccess) return cuda_fail(e, "draft_head_argmax rerank launch");
   return ok();
+}
+
+extern "C" {
+
+int dh_draft_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                         const void* S, const void* ZS, const void* W, int64_t N, int G, int bits,
+                         int kcand, int rerank, float* cand_val, int32_t* cand_id, int32_t* rr_id,
+                         float* rr_logit, int32_t* argmax_id, void* y_coarse, void* workspace,
+                         size_t ws_bytes, dh_stream_t s) {
+  return argmax_impl(x, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank, cand_val, cand_id,
+                     rr_id, rr_logit, argmax_id, y_coarse, workspace, ws_bytes, s);
 }
 
 int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
@@ -422,13 +441,37 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
     if (c.exec && c.key.v == key.v) exec = c.exec;
   if (exec == nullptr) {
     const cudaStream_t cs = hd->stream;
-    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-    if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: begin capture");
     const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
     const size_t rb = static_cast<size_t>(M) * static_cast<size_t>(rerank) * 4;
+    // Page-locked host arrays mapped into the device's address space: x is staged by a copy
+    // kernel (the coarse pass starts during it, as its programmatic dependent) and the rerank
+    // writes the results into the host arrays itself, so the graph holds kernels only.
+    // Otherwise: copy-engine transfers in and out.
+    void* xv = nullptr;
+    void* av = nullptr;
+    void* iv = nullptr;
+    void* lv = nullptr;
+    const bool mapped =
+        cudaHostGetDevicePointer(&xv, const_cast<void*>(x_host), 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&av, argmax_host, 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&iv, rr_id_host, 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&lv, rr_logit_host, 0) == cudaSuccess &&
+        aligned(xv, 16) && xb % 16 == 0;
+    if (!mapped) (void)cudaGetLastError();  // a failed lookup leaves no error behind
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: begin capture");
     int rc = DH_OK;
-    e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) {
+    if (mapped) {
+      e = dh::launch_stage_in(xv, x_dev, xb, cs);
+      if (e == cudaSuccess)
+        rc = argmax_impl(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank, cand_val,
+                         cand_id, rr_id, rr_logit, argmax_id, nullptr, workspace, ws_bytes,
+                         reinterpret_cast<dh_stream_t>(cs), static_cast<int32_t*>(av),
+                         static_cast<int32_t*>(iv), static_cast<float*>(lv));
+    } else {
+      e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, cs);
+    }
+    if (!mapped && e == cudaSuccess) {
       rc = dh_draft_head_argmax(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank,
                                 cand_val, cand_id, rr_id, rr_logit, argmax_id, nullptr,
                                 workspace, ws_bytes, reinterpret_cast<dh_stream_t>(cs));

@@ -38,6 +38,10 @@ struct RerankCall {
   uint32_t* status;
   const uint8_t* W8 = nullptr;      // e4m3 rows [N, K] instead of W (FP8 checkpoints) ...
   const float* wscale = nullptr;    // ... with their fp32 per-row scale [N]
+  // device views of page-locked host arrays written with the same results (or nullptr)
+  int32_t* h_rr_id = nullptr;
+  float* h_rr_logit = nullptr;
+  int32_t* h_argmax_id = nullptr;
 };
 
 // W bf16 [N, K], or (row_scale != nullptr) e4m3 [N, K] bytes whose values are multiplied by the
@@ -57,6 +61,10 @@ bool coarse_wide_supports(const CoarseCall& cc);
 cudaError_t launch_coarse_wide(const CoarseCall& cc, void* scratch, int num_sms, int max_smem,
                                cudaStream_t s);
 cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s);
+// Copies `bytes` (a multiple of 16; both pointers 16-byte aligned) from src, the device view of
+// page-locked host memory, to device memory; the next kernel in the stream may start its
+// programmatic-dependent prologue meanwhile (host_io.cu).
+cudaError_t launch_stage_in(const void* src, void* dst, size_t bytes, cudaStream_t s);
 // y [M, N] bf16 = -inf except y[m, rr_id[m, j]] = bf16(rr_logit[m, j]) (topk_only.cu).
 cudaError_t launch_topk_only(const int32_t* rr_id, const float* rr_logit, int64_t M, int R,
                              int64_t N, void* y, cudaStream_t s);

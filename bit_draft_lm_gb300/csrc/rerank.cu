@@ -45,6 +45,10 @@ struct RerankArgs {
   int32_t* argmax_id;  // [M]
   uint16_t* y;         // bf16 [M, N] or nullptr
   uint32_t* status;
+  // device views of page-locked host arrays that receive the same three results, or nullptr
+  int32_t* h_rr_id;
+  float* h_rr_logit;
+  int32_t* h_argmax_id;
 };
 
 // Selection order: key descending, then id ascending (as unsigned with the sign bit flipped),
@@ -369,11 +373,18 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
     }
     const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
     const uint32_t umin = __reduce_min_sync(0xffffffffu, bk == kmax ? bu : 0xffffffffu);
-    if (lane == 0) a.argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+    if (lane == 0) {
+      a.argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+      if (a.h_argmax_id) a.h_argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+    }
   }
   for (int j = tid; j < a.R; j += kRerankThreads) {
     a.rr_id[static_cast<int64_t>(m) * a.R + j] = sel_id[j];
     a.rr_logit[static_cast<int64_t>(m) * a.R + j] = sel_logit[j];
+    if (a.h_rr_id) {
+      a.h_rr_id[static_cast<int64_t>(m) * a.R + j] = sel_id[j];
+      a.h_rr_logit[static_cast<int64_t>(m) * a.R + j] = sel_logit[j];
+    }
     const int n = sel_id[j];
     if (a.y && n >= 0 && n < a.N)
       a.y[static_cast<int64_t>(m) * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sel_logit[j]));
@@ -564,6 +575,7 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     if (tid < a.R) {
       const int32_t id = sh.rr[tid];
       a.rr_id[static_cast<int64_t>(m) * a.R + tid] = id;
+      if (a.h_rr_id) a.h_rr_id[static_cast<int64_t>(m) * a.R + tid] = id;
       for (int c = 1; c < kRC; ++c) cl.map_shared_rank(sh.rr, c)[tid] = id;
     }
   }
@@ -646,6 +658,7 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
       const float v = sh.logit[j];
       const int32_t n = sh.rr[j];
       a.rr_logit[static_cast<int64_t>(m) * a.R + j] = v;
+      if (a.h_rr_logit) a.h_rr_logit[static_cast<int64_t>(m) * a.R + j] = v;
       if (a.y && n >= 0 && n < a.N)
         a.y[static_cast<int64_t>(m) * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
       const uint32_t k = order_key(v);
@@ -657,7 +670,10 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     }
     const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
     const uint32_t umin = __reduce_min_sync(0xffffffffu, bk == kmax ? bu : 0xffffffffu);
-    if (lane == 0) a.argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+    if (lane == 0) {
+      a.argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+      if (a.h_argmax_id) a.h_argmax_id[m] = static_cast<int32_t>(umin ^ 0x80000000u);
+    }
   }
 }
 
@@ -734,6 +750,9 @@ cudaError_t launch_rerank_argmax(const RerankCall& rc, cudaStream_t s) {
   a.argmax_id = rc.argmax_id;
   a.y = static_cast<uint16_t*>(rc.y);
   a.status = rc.status;
+  a.h_rr_id = rc.h_rr_id;
+  a.h_rr_logit = rc.h_rr_logit;
+  a.h_argmax_id = rc.h_argmax_id;
   return rc.W8 != nullptr ? launch_rerank_fmt<true>(a, rc, s) : launch_rerank_fmt<false>(a, rc, s);
 }
 

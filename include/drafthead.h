@@ -224,7 +224,11 @@ int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, 
  *   x_dev, cand_val, cand_id, rr_id, rr_logit, argmax_id, workspace: device buffers as for
  *   dh_draft_head_argmax (its device outputs are written too); the other arguments likewise.
  * The sequence is captured into a CUDA graph the first time an argument set is seen on a
- * device (on a stream of the library's own) and replayed on s on later calls. The library
+ * device (on a stream of the library's own) and replayed on s on later calls. When the four
+ * host arrays are mapped into the device's address space (page-locked memory on a system with
+ * unified addressing, as cudaHostAlloc gives), a copy kernel stages x (the coarse pass starts
+ * during it) and the rerank kernel writes the three results into the host arrays directly, so
+ * the graph holds kernels only; otherwise it copies with the copy engines. The library
  * keeps the 16 most recent such graphs and one capture stream per device, no device memory. Returns DH_ERR_PARAM while s is being captured; otherwise the first failing step's
  * status. A kernel-side failure is read with dh_workspace_status.
  */
