@@ -4,6 +4,7 @@
 
 #include <array>
 #include <mutex>
+#include <new>
 
 #include <cstdarg>
 #include <cstdint>
@@ -387,6 +388,127 @@ int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, 
   return ok();
 }
 
+}  // extern "C"
+
+// Checks of the host-memory call's own arguments (the device calls it makes check the rest).
+static int check_host(const char* who, const void* x_host, int64_t M, int64_t K, void* x_dev,
+                      int rerank, int32_t* argmax_host, int32_t* rr_id_host,
+                      float* rr_logit_host) {
+  if (!x_host || !x_dev || !argmax_host || !rr_id_host || !rr_logit_host)
+    return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  if (M < 1 || M > DH_MAX_TOKENS || K < 1 || rerank < 1 || rerank > DH_MAX_RERANK)
+    return fail(DH_ERR_SHAPE, "%s: M=%lld K=%lld rerank=%d", who, (long long)M, (long long)K,
+                rerank);
+  if (!aligned(x_dev, 16)) return fail(DH_ERR_ALIGN, "%s: x_dev must be 16-byte aligned", who);
+  return DH_OK;
+}
+
+static int check_not_capturing(const char* who, cudaStream_t us) {
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(us, &cap_status);
+  if (e != cudaSuccess) return cuda_fail(e, "stream query");
+  if (cap_status != cudaStreamCaptureStatusNone)
+    return fail(DH_ERR_PARAM, "%s: the stream is being captured (this call synchronises)", who);
+  return DH_OK;
+}
+
+// The host-memory call captured into an executable graph on device dev's capture stream (a
+// capture cannot run on the legacy default stream). Caller holds g_host_mu.
+static int capture_host_call(int dev, const void* x_host, int64_t M, int64_t K, void* x_dev,
+                             const uint8_t* packed, const void* S, const void* ZS, const void* W,
+                             int64_t N, int G, int bits, int kcand, int rerank, float* cand_val,
+                             int32_t* cand_id, int32_t* rr_id, float* rr_logit,
+                             int32_t* argmax_id, int32_t* argmax_host, int32_t* rr_id_host,
+                             float* rr_logit_host, void* workspace, size_t ws_bytes,
+                             cudaGraphExec_t* out) {
+  HostDevice* hd = nullptr;
+  cudaError_t e = host_device(dev, &hd);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: stream creation");
+  const cudaStream_t cs = hd->stream;
+  const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
+  const size_t rb = static_cast<size_t>(M) * static_cast<size_t>(rerank) * 4;
+  // Page-locked host arrays mapped into the device's address space: x is staged by a copy
+  // kernel (the coarse pass starts during it, as its programmatic dependent) and the rerank
+  // writes the results into the host arrays itself, so the graph holds kernels only.
+  // Otherwise: copy-engine transfers in and out.
+  void* xv = nullptr;
+  void* av = nullptr;
+  void* iv = nullptr;
+  void* lv = nullptr;
+  const bool mapped =
+      cudaHostGetDevicePointer(&xv, const_cast<void*>(x_host), 0) == cudaSuccess &&
+      cudaHostGetDevicePointer(&av, argmax_host, 0) == cudaSuccess &&
+      cudaHostGetDevicePointer(&iv, rr_id_host, 0) == cudaSuccess &&
+      cudaHostGetDevicePointer(&lv, rr_logit_host, 0) == cudaSuccess && aligned(xv, 16) &&
+      xb % 16 == 0;
+  if (!mapped) (void)cudaGetLastError();  // a failed lookup leaves no error behind
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: begin capture");
+  int rc = DH_OK;
+  const dh_stream_t ds = reinterpret_cast<dh_stream_t>(cs);
+  if (mapped) {
+    e = dh::launch_stage_in(xv, x_dev, xb, cs);
+    if (e == cudaSuccess)
+      rc = argmax_impl(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank, cand_val,
+                       cand_id, rr_id, rr_logit, argmax_id, nullptr, workspace, ws_bytes, ds,
+                       static_cast<int32_t*>(av), static_cast<int32_t*>(iv),
+                       static_cast<float*>(lv));
+  } else {
+    e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess)
+      rc = argmax_impl(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank, cand_val,
+                       cand_id, rr_id, rr_logit, argmax_id, nullptr, workspace, ws_bytes, ds);
+    if (e == cudaSuccess && rc == DH_OK) {
+      // one copy when the three results lie back to back on both sides (argmax, rr_id,
+      // rr_logit), else three
+      const size_t ab = static_cast<size_t>(M) * 4;
+      auto* dv = reinterpret_cast<const unsigned char*>(argmax_id);
+      auto* hv = reinterpret_cast<unsigned char*>(argmax_host);
+      const bool joint = reinterpret_cast<const unsigned char*>(rr_id) == dv + ab &&
+                         reinterpret_cast<const unsigned char*>(rr_logit) == dv + ab + rb &&
+                         reinterpret_cast<unsigned char*>(rr_id_host) == hv + ab &&
+                         reinterpret_cast<unsigned char*>(rr_logit_host) == hv + ab + rb;
+      if (joint) {
+        e = cudaMemcpyAsync(hv, dv, ab + 2 * rb, cudaMemcpyDeviceToHost, cs);
+      } else {
+        e = cudaMemcpyAsync(argmax_host, argmax_id, ab, cudaMemcpyDeviceToHost, cs);
+        if (e == cudaSuccess)
+          e = cudaMemcpyAsync(rr_id_host, rr_id, rb, cudaMemcpyDeviceToHost, cs);
+        if (e == cudaSuccess)
+          e = cudaMemcpyAsync(rr_logit_host, rr_logit, rb, cudaMemcpyDeviceToHost, cs);
+      }
+    }
+  }
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ee = cudaStreamEndCapture(cs, &graph);
+  if (rc != DH_OK || e != cudaSuccess || ee != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != DH_OK) return rc;  // the failing call recorded its message
+    return cuda_fail(e != cudaSuccess ? e : ee, "draft_head_host: capture");
+  }
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: instantiate");
+  *out = exec;
+  return DH_OK;
+}
+
+// Replays an executable graph of the host-memory call on s and waits for it.
+static int run_host_graph(cudaGraphExec_t exec, cudaStream_t us) {
+  cudaError_t e = cudaGraphLaunch(exec, us);  // stream-ordered after the caller's earlier work
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: launch");
+  e = cudaStreamSynchronize(us);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: synchronise");
+  return ok();
+}
+
+struct dh_host_plan_s {
+  cudaGraphExec_t exec;
+};
+
+extern "C" {
+
 int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
                        const uint8_t* packed, const void* S, const void* ZS, const void* W,
                        int64_t N, int G, int bits, int kcand, int rerank, float* cand_val,
@@ -394,25 +516,16 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
                        int32_t* argmax_host, int32_t* rr_id_host, float* rr_logit_host,
                        void* workspace, size_t ws_bytes, dh_stream_t s) {
   const char* who = "draft_head_host";
-  if (!x_host || !x_dev || !argmax_host || !rr_id_host || !rr_logit_host)
-    return fail(DH_ERR_NULL, "%s: NULL pointer", who);
-  if (M < 1 || M > DH_MAX_TOKENS || K < 1 || rerank < 1 || rerank > DH_MAX_RERANK)
-    return fail(DH_ERR_SHAPE, "%s: M=%lld K=%lld rerank=%d", who, (long long)M, (long long)K,
-                rerank);
-  if (!aligned(x_dev, 16)) return fail(DH_ERR_ALIGN, "%s: x_dev must be 16-byte aligned", who);
+  int rc = check_host(who, x_host, M, K, x_dev, rerank, argmax_host, rr_id_host, rr_logit_host);
+  if (rc != DH_OK) return rc;
   cudaStream_t us = reinterpret_cast<cudaStream_t>(s);
-  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(us, &cap_status);
-  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: stream query");
-  if (cap_status != cudaStreamCaptureStatusNone)
-    return fail(DH_ERR_PARAM, "%s: the stream is being captured (this call synchronises)", who);
+  rc = check_not_capturing(who, us);
+  if (rc != DH_OK) return rc;
   int dev = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: device query");
 
-  // The whole sequence once per distinct argument set and device: captured into a graph on a
-  // stream of the library's own (a capture cannot run on the legacy default stream), then
-  // replayed on s itself.
+  // The whole sequence once per distinct argument set and device, then replayed on s itself.
   HostGraphKey key{};
   const uint64_t vals[] = {reinterpret_cast<uint64_t>(x_host), static_cast<uint64_t>(M),
                            static_cast<uint64_t>(K), reinterpret_cast<uint64_t>(x_dev),
@@ -433,90 +546,65 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
   for (size_t i = 0; i < sizeof(vals) / sizeof(vals[0]); ++i) key.v[i] = vals[i];
 
   std::lock_guard<std::mutex> lock(g_host_mu);
-  HostDevice* hd = nullptr;
-  e = host_device(dev, &hd);
-  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: stream creation");
   cudaGraphExec_t exec = nullptr;
   for (auto& c : g_host_graphs)
     if (c.exec && c.key.v == key.v) exec = c.exec;
   if (exec == nullptr) {
-    const cudaStream_t cs = hd->stream;
-    const size_t xb = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
-    const size_t rb = static_cast<size_t>(M) * static_cast<size_t>(rerank) * 4;
-    // Page-locked host arrays mapped into the device's address space: x is staged by a copy
-    // kernel (the coarse pass starts during it, as its programmatic dependent) and the rerank
-    // writes the results into the host arrays itself, so the graph holds kernels only.
-    // Otherwise: copy-engine transfers in and out.
-    void* xv = nullptr;
-    void* av = nullptr;
-    void* iv = nullptr;
-    void* lv = nullptr;
-    const bool mapped =
-        cudaHostGetDevicePointer(&xv, const_cast<void*>(x_host), 0) == cudaSuccess &&
-        cudaHostGetDevicePointer(&av, argmax_host, 0) == cudaSuccess &&
-        cudaHostGetDevicePointer(&iv, rr_id_host, 0) == cudaSuccess &&
-        cudaHostGetDevicePointer(&lv, rr_logit_host, 0) == cudaSuccess &&
-        aligned(xv, 16) && xb % 16 == 0;
-    if (!mapped) (void)cudaGetLastError();  // a failed lookup leaves no error behind
-    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-    if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: begin capture");
-    int rc = DH_OK;
-    if (mapped) {
-      e = dh::launch_stage_in(xv, x_dev, xb, cs);
-      if (e == cudaSuccess)
-        rc = argmax_impl(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank, cand_val,
-                         cand_id, rr_id, rr_logit, argmax_id, nullptr, workspace, ws_bytes,
-                         reinterpret_cast<dh_stream_t>(cs), static_cast<int32_t*>(av),
-                         static_cast<int32_t*>(iv), static_cast<float*>(lv));
-    } else {
-      e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, cs);
-    }
-    if (!mapped && e == cudaSuccess) {
-      rc = dh_draft_head_argmax(x_dev, M, K, packed, S, ZS, W, N, G, bits, kcand, rerank,
-                                cand_val, cand_id, rr_id, rr_logit, argmax_id, nullptr,
-                                workspace, ws_bytes, reinterpret_cast<dh_stream_t>(cs));
-      if (rc == DH_OK) {
-        // one copy when the three results lie back to back on both sides (argmax, rr_id,
-        // rr_logit), else three
-        const size_t ab = static_cast<size_t>(M) * 4;
-        auto* dv = reinterpret_cast<const unsigned char*>(argmax_id);
-        auto* hv = reinterpret_cast<unsigned char*>(argmax_host);
-        const bool joint = reinterpret_cast<const unsigned char*>(rr_id) == dv + ab &&
-                           reinterpret_cast<const unsigned char*>(rr_logit) == dv + ab + rb &&
-                           reinterpret_cast<unsigned char*>(rr_id_host) == hv + ab &&
-                           reinterpret_cast<unsigned char*>(rr_logit_host) == hv + ab + rb;
-        if (joint) {
-          e = cudaMemcpyAsync(hv, dv, ab + 2 * rb, cudaMemcpyDeviceToHost, cs);
-        } else {
-          e = cudaMemcpyAsync(argmax_host, argmax_id, ab, cudaMemcpyDeviceToHost, cs);
-          if (e == cudaSuccess)
-            e = cudaMemcpyAsync(rr_id_host, rr_id, rb, cudaMemcpyDeviceToHost, cs);
-          if (e == cudaSuccess)
-            e = cudaMemcpyAsync(rr_logit_host, rr_logit, rb, cudaMemcpyDeviceToHost, cs);
-        }
-      }
-    }
-    cudaGraph_t graph = nullptr;
-    const cudaError_t ee = cudaStreamEndCapture(cs, &graph);
-    if (rc != DH_OK || e != cudaSuccess || ee != cudaSuccess) {
-      if (graph) cudaGraphDestroy(graph);
-      if (rc != DH_OK) return rc;  // the failing call recorded its message
-      return cuda_fail(e != cudaSuccess ? e : ee, "draft_head_host: capture");
-    }
-    e = cudaGraphInstantiate(&exec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: instantiate");
+    rc = capture_host_call(dev, x_host, M, K, x_dev, packed, S, ZS, W, N, G, bits, kcand, rerank,
+                           cand_val, cand_id, rr_id, rr_logit, argmax_id, argmax_host,
+                           rr_id_host, rr_logit_host, workspace, ws_bytes, &exec);
+    if (rc != DH_OK) return rc;
     HostGraph& slot = g_host_graphs[g_host_next];
     g_host_next = (g_host_next + 1) % kHostGraphs;
     if (slot.exec) cudaGraphExecDestroy(slot.exec);  // the oldest argument set
     slot.key = key;
     slot.exec = exec;
   }
-  e = cudaGraphLaunch(exec, us);  // stream-ordered after the caller's earlier work on s
-  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: launch");
-  e = cudaStreamSynchronize(us);
-  if (e != cudaSuccess) return cuda_fail(e, "draft_head_host: synchronise");
+  return run_host_graph(exec, us);
+}
+
+int dh_host_plan_create(const void* x_host, int64_t M, int64_t K, void* x_dev,
+                        const uint8_t* packed, const void* S, const void* ZS, const void* W,
+                        int64_t N, int G, int bits, int kcand, int rerank, float* cand_val,
+                        int32_t* cand_id, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                        int32_t* argmax_host, int32_t* rr_id_host, float* rr_logit_host,
+                        void* workspace, size_t ws_bytes, dh_host_plan* plan) {
+  const char* who = "host_plan_create";
+  if (!plan) return fail(DH_ERR_NULL, "%s: NULL plan pointer", who);
+  *plan = nullptr;
+  int rc = check_host(who, x_host, M, K, x_dev, rerank, argmax_host, rr_id_host, rr_logit_host);
+  if (rc != DH_OK) return rc;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "host_plan_create: device query");
+  dh_host_plan p = new (std::nothrow) dh_host_plan_s{nullptr};
+  if (!p) return fail(DH_ERR_PARAM, "%s: out of host memory", who);
+  {
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    rc = capture_host_call(dev, x_host, M, K, x_dev, packed, S, ZS, W, N, G, bits, kcand, rerank,
+                           cand_val, cand_id, rr_id, rr_logit, argmax_id, argmax_host,
+                           rr_id_host, rr_logit_host, workspace, ws_bytes, &p->exec);
+  }
+  if (rc != DH_OK) {
+    delete p;
+    return rc;
+  }
+  *plan = p;
   return ok();
+}
+
+int dh_host_plan_run(dh_host_plan plan, dh_stream_t s) {
+  if (!plan) return fail(DH_ERR_NULL, "host_plan_run: NULL plan");
+  cudaStream_t us = reinterpret_cast<cudaStream_t>(s);
+  const int rc = check_not_capturing("host_plan_run", us);
+  if (rc != DH_OK) return rc;
+  return run_host_graph(plan->exec, us);
+}
+
+void dh_host_plan_destroy(dh_host_plan plan) {
+  if (!plan) return;
+  cudaGraphExecDestroy(plan->exec);
+  delete plan;
 }
 
 int dh_workspace_status(const void* workspace, size_t ws_bytes, uint32_t* device_status,

@@ -49,6 +49,10 @@ SIGNATURES = {
                                              _P, _P, _P, _P], _I),
     "dh_draft_head_host": ([_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
                             _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "dh_host_plan_create": ([_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P,
+                             _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "dh_host_plan_run": ([_P, _P], _I),
+    "dh_host_plan_destroy": ([_P], None),
     "dh_topk_only_logits": ([_P, _P, _I64, _I, _I64, _P, _P], _I),
     "dh_quantize_pack_int2_fp8": ([_P, _P, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "dh_draft_head_rerank_argmax_fp8": ([_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _I, _P, _P,
@@ -419,14 +423,16 @@ class DraftHead:
         s.synchronize()
         return g["h_am"], g["h_rr"], g["h_rl"]
 
-    def call_host(self, x_host: torch.Tensor, stream=None):
-        """The same end-to-end call through the library's host-memory entry point
-        (dh_draft_head_host): copy in, coarse pass, rerank, copies out and the synchronisation
-        all happen in native code. Returns pinned host tensors (argmax [M], rr_id [M, R],
-        rr_logit [M, R]), views of buffers the next call with the same M overwrites."""
+    def call_host(self, x_host: torch.Tensor, stream=None, plan: bool = True):
+        """The same end-to-end call through the library's host-memory entry points: copy in,
+        coarse pass, rerank, results out and the synchronisation all happen in native code.
+        plan=True (default): a dh_host_plan prepared on the first call per (M, x_host) and run
+        with dh_host_plan_run; plan=False: dh_draft_head_host with every argument each call.
+        Returns pinned host tensors (argmax [M], rr_id [M, R], rr_logit [M, R]), views of
+        buffers the next call with the same M overwrites."""
         M, R = x_host.shape[0], self.rerank
         sh = _stream(stream)
-        key = (M, x_host.data_ptr(), sh)
+        key = (M, x_host.data_ptr())
         cached = self._host_calls.get(key) if hasattr(self, "_host_calls") else None
         if cached is None:
             if M < 1 or M > self.max_tokens:
@@ -436,7 +442,7 @@ class DraftHead:
                 raise ValueError("x_host must be a contiguous host tensor [M, K]")
             if not hasattr(self, "_host_bufs"):
                 dev, n = self.W.device, self.max_tokens * (1 + 2 * R)
-                # results back to back (argmax, rr_id, rr_logit) on both sides: one copy out
+                # results back to back (argmax, rr_id, rr_logit) on both sides
                 self._host_bufs = (
                     torch.empty(self.max_tokens, self.K, dtype=torch.bfloat16, device=dev),
                     torch.empty(n, dtype=torch.int32, device=dev),
@@ -452,11 +458,27 @@ class DraftHead:
                     self.S.data_ptr(), self.ZS.data_ptr(), self.W.data_ptr(), self.N, self.G,
                     self.bits, self.kcand, R, self._cv.data_ptr(), self._ci.data_ptr(),
                     d_rr.data_ptr(), d_rl.data_ptr(), d_am.data_ptr(), h_am.data_ptr(),
-                    h_rr.data_ptr(), h_rl.data_ptr(), ws.data_ptr(), ws.numel(), sh)
-            cached = (args, (h_am, h_rr, h_rl), x_host)  # x_host kept alive with its pointer
+                    h_rr.data_ptr(), h_rl.data_ptr(), ws.data_ptr(), ws.numel())
+            handle = ctypes.c_void_p()
+            _check(lib().dh_host_plan_create(*args, ctypes.byref(handle)))
+            # x_host is kept alive with its pointer; the plan is freed with this object
+            cached = (args, (h_am, h_rr, h_rl), x_host, handle)
             self._host_calls[key] = cached
-        _check(lib().dh_draft_head_host(*cached[0]))
+        if plan:
+            _check(lib().dh_host_plan_run(cached[3], sh))
+        else:
+            _check(lib().dh_draft_head_host(*cached[0], sh))
         return cached[1]
+
+    def __del__(self):
+        calls = getattr(self, "_host_calls", None)
+        if calls and _lib is not None:
+            for c in calls.values():
+                try:
+                    _lib.dh_host_plan_destroy(c[3])
+                except Exception:
+                    pass
+            calls.clear()
 
     def _build_infer_graph(self, M: int) -> dict:
         dev, R = self.W.device, self.rerank

@@ -240,6 +240,28 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
                        void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
+ * A host-memory call prepared once: dh_host_plan_create validates the arguments of
+ * dh_draft_head_host (all but the stream) and captures the call into a CUDA graph that the plan
+ * owns (on the current device); dh_host_plan_run replays it on s and synchronises s, so that a
+ * repeated call passes two arguments instead of twenty-four. The buffers stay bound to the plan:
+ * write the next x into the same x_host, read the results from the same host arrays.
+ *   dh_host_plan_create: *plan = NULL on failure (the first failing check's status, as for
+ *     dh_draft_head_host); the library keeps no reference to the plan.
+ *   dh_host_plan_run: DH_ERR_NULL for a NULL plan, DH_ERR_PARAM while s is being captured;
+ *     run it with the device current that the plan was created on.
+ *   dh_host_plan_destroy: frees the plan and its graph (NULL is ignored); not while it runs.
+ */
+typedef struct dh_host_plan_s* dh_host_plan;
+int dh_host_plan_create(const void* x_host, int64_t M, int64_t K, void* x_dev,
+                        const uint8_t* packed, const void* S, const void* ZS, const void* W,
+                        int64_t N, int G, int bits, int kcand, int rerank, float* cand_val,
+                        int32_t* cand_id, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                        int32_t* argmax_host, int32_t* rr_id_host, float* rr_logit_host,
+                        void* workspace, size_t ws_bytes, dh_host_plan* plan);
+int dh_host_plan_run(dh_host_plan plan, dh_stream_t s);
+void dh_host_plan_destroy(dh_host_plan plan);
+
+/*
  * Synchronises `s`, copies the workspace status word to *device_status and returns DH_OK if
  * it is zero, DH_ERR_DEVICE otherwise (DH_ERR_CUDA if the copy fails). The word is sticky:
  * zero the workspace to clear it.

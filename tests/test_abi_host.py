@@ -191,3 +191,25 @@ def test_argmax_call_validation(lib):
     assert f(*bad) == dh.DH_ERR_ALIGN
     bad = list(args); bad[19] = 128      # smaller than the 256-byte header
     assert f(*bad) == dh.DH_ERR_WORKSPACE
+
+
+def test_host_plan_validation(lib):
+    """dh_host_plan_create rejects bad arguments before any CUDA call and leaves *plan NULL;
+    dh_host_plan_run rejects a NULL plan; dh_host_plan_destroy ignores NULL."""
+    f = lib.dh_host_plan_create
+    args = [A16, 1, 1024, A16, A16, A16, A16, A16, 8192, 128, 2, 8, 16, A16, A16, A16, A16, A16,
+            A16, A16, A16, A256, 256]
+    plan = ctypes.c_void_p(0x1234)
+    bad = list(args); bad[0] = None      # x_host
+    assert f(*bad, ctypes.byref(plan)) == dh.DH_ERR_NULL and plan.value is None
+    assert f(*args, None) == dh.DH_ERR_NULL
+    bad = list(args); bad[18] = None     # argmax_host
+    assert f(*bad, ctypes.byref(plan)) == dh.DH_ERR_NULL
+    bad = list(args); bad[1] = 0         # M
+    assert f(*bad, ctypes.byref(plan)) == dh.DH_ERR_SHAPE
+    bad = list(args); bad[12] = 300      # rerank
+    assert f(*bad, ctypes.byref(plan)) == dh.DH_ERR_SHAPE
+    bad = list(args); bad[3] = A16 + 4   # x_dev misaligned
+    assert f(*bad, ctypes.byref(plan)) == dh.DH_ERR_ALIGN
+    assert lib.dh_host_plan_run(None, None) == dh.DH_ERR_NULL
+    lib.dh_host_plan_destroy(None)

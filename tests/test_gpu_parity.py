@@ -321,8 +321,9 @@ def test_draft_head_infer_from_host():
 
 
 def test_draft_head_host_entry_point():
-    """dh_draft_head_host (copy in, coarse, rerank, copies out, synchronise, all native) returns
-    the same results as the device-side call and as the graph-replayed infer."""
+    """The host-memory call (x in, coarse, rerank, results out, synchronise, all native), through a
+    dh_host_plan and through dh_draft_head_host, returns the same results as the device-side
+    call and as the graph-replayed infer."""
     w = synth.make_workload(2, 1024, 8192, 42, plant=True)
     W = dev_bf16(w.W)
     head = dh.DraftHead(W, 128, 2, 8, 16, max_tokens=2)
@@ -336,6 +337,9 @@ def test_draft_head_host_entry_point():
         assert torch.equal(am, ref["argmax"].cpu())
         assert torch.equal(rr, ref["rr_id"].cpu())
         assert torch.equal(rl, ref["rr_logit"].cpu())
+        # the same call through dh_draft_head_host with every argument (its graph cache)
+        dam, drr, drl = (t.clone() for t in head.call_host(x_host, plan=False))
+        assert torch.equal(am, dam) and torch.equal(rr, drr) and torch.equal(rl, drl)
         gam, grr, grl = head.infer(x_host)
         assert torch.equal(am, gam) and torch.equal(rr, grr) and torch.equal(rl, grl)
     assert dh.dh_workspace_status(head.workspace) == 0
