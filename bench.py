@@ -368,9 +368,10 @@ def extra_ms(args):
 
 
 def run_e2e(args, dev, Ws, xs_h, ncopy):
-    """The C-ABI call with host buffers: dh_draft_head_host (through DraftHead.call_host) copies x
-    from pinned host memory, runs the head and copies argmax / rr_id / rr_logit back, then
-    synchronises, every step. The graph-replayed DraftHead.infer is timed beside it."""
+    """The C-ABI call with host buffers (DraftHead.call_host: a dh_host_plan run every step, which
+    takes x from pinned host memory, runs the head, puts argmax / rr_id / rr_logit into pinned
+    host memory and synchronises). dh_draft_head_host with all its arguments and the
+    graph-replayed DraftHead.infer are timed beside it."""
     import torch
     from bit_draft_lm_gb300 import drafthead as dh
     M = args.m
@@ -389,13 +390,15 @@ def run_e2e(args, dev, Ws, xs_h, ncopy):
         return (time.perf_counter() - t0) * 1e6 / steps
 
     v = timed(lambda h, x: h.call_host(x))
+    d = timed(lambda h, x: h.call_host(x, plan=False))
     g = timed(lambda h, x: h.infer(x))
     for h in heads:
         if dh.dh_workspace_status(h.workspace):
             raise RuntimeError("kernel status word set in the end-to-end run")
     return {"value": round(v, 3), "unit": "us/call", "h2d_bytes_per_step": M * K_DIM * 2,
             "d2h_bytes_per_step": M * 4 + 2 * M * RERANK * 4, "steps": steps,
-            "api": "dh_draft_head_host (C ABI, host buffers)",
+            "api": "dh_host_plan_run (C ABI, host buffers; plan prepared once per M)",
+            "direct_call_value": round(d, 3),
             "graph_replay_value": round(g, 3)}
 
 
