@@ -213,3 +213,25 @@ def test_host_plan_validation(lib):
     assert f(*bad, ctypes.byref(plan)) == dh.DH_ERR_ALIGN
     assert lib.dh_host_plan_run(None, None) == dh.DH_ERR_NULL
     lib.dh_host_plan_destroy(None)
+
+
+def test_binding_rejects_host_tensors_and_bad_dtypes(lib):
+    """The Python binding refuses CPU tensors, non-bf16 inputs and mis-shaped outputs before it
+    calls into the library (the CPU-tensor guard of the page's plug-in tests)."""
+    import torch
+    x = torch.zeros(1, 1024, dtype=torch.bfloat16)
+    W = torch.zeros(8192, 1024, dtype=torch.bfloat16)
+    packed = torch.zeros(8192, 256, dtype=torch.uint8)
+    S = torch.zeros(8192, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dh.dh_draft_head_coarse_topk(x, packed, S, S, 8192)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dh.dh_draft_head_argmax(x, packed, S, S, W)
+    cv = torch.zeros(1, 1024, dtype=torch.float32)
+    ci = torch.zeros(1, 1024, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dh.dh_draft_head_rerank_argmax(x, W, cv, ci, 16)
+    with pytest.raises(ValueError, match="bf16"):
+        dh.dh_draft_head_rerank_argmax(x.float(), W, cv, ci, 16)
+    with pytest.raises(ValueError, match="bf16"):
+        dh.dh_quantize_pack_int2(W.float())
