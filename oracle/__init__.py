@@ -53,8 +53,10 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB)
+        # ORACLE_LIB: another build of oracle.c, for the pin tests' planted-mistake (mutant)
+        # check; normally unset
+        path = os.environ.get("ORACLE_LIB") or build()
+        lib = ctypes.CDLL(path)
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         I = ctypes.c_int

@@ -231,7 +231,8 @@ def _brute_block_topk(c, kcand):
     return val, ids
 
 
-@pytest.mark.parametrize("N,kcand", [(640, 8), (700, 8), (130, 1), (64, 64), (200, 3)])
+@pytest.mark.parametrize("N,kcand", [(640, 8), (700, 8), (130, 1), (64, 64), (200, 3),
+                                     (70, 8), (130, 4)])  # last block shorter than KCAND
 def test_block_topk_brute_force(N, kcand):
     """Block top-KCAND by successive max-and-mask (_emit) == sorting each 64-row block by
     (value desc, id asc); short last block padded with (-inf, -1); ties present."""
