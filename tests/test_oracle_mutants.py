@@ -1,10 +1,15 @@
 """The oracle's pins catch planted mistakes (CPU only).
 
-Each case below plants one plausible mistake in a copy of oracle/oracle.c (a dropped term, a
-wrong sign, a wrong index or layout, a swapped operand, a wrong tie-break or rounding), builds it
-with the oracle's own compiler flags and runs tests/test_oracle_pins.py against it through the
-ORACLE_LIB hook: every mutant must fail at least one pin. The unmodified source passes them (the
-pin file itself runs in this suite).
+Each case below plants one plausible mistake (a dropped term, a wrong sign, a wrong index or
+layout, a swapped operand, a wrong tie-break or rounding) in a copy of the oracle and runs
+tests/test_oracle_pins.py against it: every mutant must fail at least one pin.
+- C mutants of oracle/oracle.c are built with the oracle's own compiler flags and loaded through
+  the ORACLE_LIB hook.
+- Python mutants of oracle/__init__.py (the e4m3 decode, the FP8 quantiser's input, the FP8
+  rerank, bf16 rounding, the top-K logits) are loaded as the `oracle` module through the
+  ORACLE_PY hook of tests/conftest.py.
+The unmodified sources pass the pins (the pin file itself runs in this suite, and a fresh build
+of the unmodified C source is checked below).
 """
 import os
 import subprocess
@@ -52,6 +57,28 @@ MUTANTS = [
 ]
 
 
+PY_SRC = os.path.join(ROOT, "oracle", "__init__.py")
+
+# (name, text in oracle/__init__.py, replacement)
+PY_MUTANTS = [
+    ("e4m3: subnormal step 2^-10",
+     "m * 2.0 ** -9, (1.0", "m * 2.0 ** -10, (1.0"),
+    ("e4m3: exponent bias 8",
+     "np.exp2((e - 7).astype(np.float64))", "np.exp2((e - 8).astype(np.float64))"),
+    ("e4m3: sign from bit 6",
+     "np.where((b & 128) != 0, -mag, mag)", "np.where((b & 64) != 0, -mag, mag)"),
+    ("bf16 rounding: ties away from zero",
+     "((u + 0x7FFF + ((u >> 16) & 1)) >> 16)", "((u + 0x8000) >> 16)"),
+    ("top-K logits: +inf fill",
+     "y = np.full((M, N), 0xFF80, dtype=np.uint16)", "y = np.full((M, N), 0x7F80, dtype=np.uint16)"),
+    ("FP8 quantiser: row scale not applied",
+     "e4m3_decode(W8).astype(np.float32) *\n                              np.asarray(scale, dtype=np.float32)[:, None]",
+     "e4m3_decode(W8).astype(np.float32) *\n                              np.float32(1.0)"),
+    ("FP8 rerank: row scale dropped",
+     "e4m3_decode(W8[n])) * float(scale[n]))", "e4m3_decode(W8[n])))"),
+]
+
+
 def _build(src_text, out):
     c = out + ".c"
     with open(c, "w") as f:
@@ -60,8 +87,10 @@ def _build(src_text, out):
                            "-fPIC", "-shared", "-pthread", "-o", out, c, "-lm"])
 
 
-def _pins_fail(lib_path):
-    env = dict(os.environ, ORACLE_LIB=lib_path)
+def _pins_fail(lib_path, py_path=None):
+    env = dict(os.environ, ORACLE_LIB=lib_path) if lib_path else dict(os.environ)
+    if py_path:
+        env["ORACLE_PY"] = py_path
     r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return r.returncode != 0, r.stdout[-400:]
@@ -88,3 +117,21 @@ def test_unmodified_copy_passes_the_pins(tmp_path):
     _build(open(SRC).read(), out)
     failed, tail = _pins_fail(out)
     assert not failed, tail
+
+
+def test_every_planted_python_mistake_fails_a_pin(tmp_path):
+    src = open(PY_SRC).read()
+    c_src = open(SRC).read()
+    paths = []
+    for i, (name, old, new) in enumerate(PY_MUTANTS):
+        old, new = old.replace("\\n", "\n"), new.replace("\\n", "\n")
+        assert src.count(old) == 1, f"mutation site not unique or missing: {name}"
+        d = tmp_path / f"pymut{i}"
+        d.mkdir()
+        (d / "__init__.py").write_text(src.replace(old, new))
+        (d / "oracle.c").write_text(c_src)  # the mutant package builds its own library copy
+        paths.append(str(d / "__init__.py"))
+    with ThreadPoolExecutor(max_workers=4) as pool:
+        results = list(pool.map(lambda p: _pins_fail(None, p), paths))
+    survived = [name for (name, _, _), (failed, _) in zip(PY_MUTANTS, results) if not failed]
+    assert not survived, "mutants the pins did not catch: " + "; ".join(survived)
