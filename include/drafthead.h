@@ -240,7 +240,8 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
                        void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
- * A host-memory call prepared once: dh_host_plan_create validates the arguments of
+ * A host-memory call prepared once (the page's _apply_head_int2 end to end, as
+ * dh_draft_head_host): dh_host_plan_create validates the arguments of
  * dh_draft_head_host (all but the stream) and captures the call into a CUDA graph that the plan
  * owns (on the current device); dh_host_plan_run replays it on s and synchronises s, so that a
  * repeated call passes two arguments instead of twenty-four. The buffers stay bound to the plan:
