@@ -173,6 +173,19 @@ static int check_rerank(const char* who, const void* x, int64_t M, int64_t K, co
   return DH_OK;
 }
 
+namespace dh {
+// The argument checks of dh_draft_head_rerank_argmax (bf16 rows), for the entry points defined in
+// other files of the library; records the message and returns the status.
+int check_rerank_call(const char* who, const void* x, int64_t M, int64_t K, const void* W,
+                      int64_t N, const float* cand_val, const int32_t* cand_id, int64_t ncand,
+                      int rerank, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                      void* y_coarse) {
+  if (!W) return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  return check_rerank(who, x, M, K, W, nullptr, nullptr, N, cand_val, cand_id, ncand, rerank,
+                      rr_id, rr_logit, argmax_id, y_coarse);
+}
+}  // namespace dh
+
 static int rerank_impl(const char* who, const void* x, int64_t M, int64_t K, const void* W,
                        const uint8_t* W8, const float* wscale, int64_t N, const float* cand_val,
                        const int32_t* cand_id, int64_t ncand, int rerank, int32_t* rr_id,

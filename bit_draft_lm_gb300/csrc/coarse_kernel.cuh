@@ -196,7 +196,13 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     *jobs_claimed = 0;
     *abort_flag = 0;
     mbar_fence_init();
-    for (int lb = 0; lb < a.nsb && lb < my_blocks; ++lb) issue_sz(lb);
+    // the first S/ZS stages into L2 only (see the weight prefetch below); copied after the wait
+    for (int lb = 0; lb < a.nsb && lb < my_blocks; ++lb) {
+      const int row0 = block_row0(lb);
+      const int rows = a.N - row0 > kBlockRows ? kBlockRows : a.N - row0;
+      prefetch_l2_bulk(a.S + static_cast<int64_t>(row0) * KG, static_cast<uint32_t>(rows * KG * 2));
+      prefetch_l2_bulk(a.ZS + static_cast<int64_t>(row0) * KG, static_cast<uint32_t>(rows * KG * 2));
+    }
   }
 
   // ---- weight streaming of tile tau = 4 lb + t into ring stage tau % NSW, by warp `warp` alone:
@@ -250,19 +256,36 @@ __global__ void __launch_bounds__(kCoarseMaxThreads, 1) coarse_topk_kernel(const
     cp_async_commit();  // one group per tile slot, possibly empty, keeps the counting uniform
   };
   // ---- weight prefetch: the first NSW - 1 tiles of this warp's strip (and, above, the S/ZS
-  // stages). The weights are not an output of the kernel that precedes this one in the stream
-  // when that kernel lets its dependents start early (this library's rerank and coarse
-  // kernels), so they are read before the wait below; a kernel that does not trigger early has
-  // completed before this one starts.
+  // stages) are fetched into L2 while the preceding kernel may still run. Only L2: the
+  // preceding kernel's writes are guaranteed visible after griddepcontrol.wait alone, and it
+  // may be the one that wrote the weights (the quantiser, or a caller's kernel); L2 is coherent,
+  // so warming it early is safe, and the copies into shared memory come after the wait.
+  {
+    const BlkSrc b0 = blk_src(0), b1 = blk_src(1);
+#pragma unroll
+    for (int t = 0; t < NSW - 1; ++t) {
+      const BlkSrc& b = t / kTilesPerBlock ? b1 : b0;
+      const int tk = t % kTilesPerBlock;
+      if (!b.live) continue;
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int rj = min(b.row0 + tk * kTileRows + r0l + j * RPJ, a.N - 1);
+        prefetch_l2(a.packed + static_cast<int64_t>(rj) * RB + src_lane);
+      }
+    }
+  }
+  // Launched as a programmatic dependent: everything below (the weights into shared memory, x,
+  // the outputs) waits for the preceding kernel's completion and the visibility of its writes
+  // (a no-op after an ordinary launch).
+  grid_dependency_wait();
+  if (threadIdx.x == 0)
+    for (int lb = 0; lb < a.nsb && lb < my_blocks; ++lb) issue_sz(lb);
   {
     const BlkSrc b0 = blk_src(0), b1 = blk_src(1);
 #pragma unroll
     for (int t = 0; t < NSW - 1; ++t)
       load_tile(t / kTilesPerBlock ? b1 : b0, t / kTilesPerBlock, t % kTilesPerBlock);
   }
-  // Launched as a programmatic dependent: everything below (x, the outputs) waits for the
-  // preceding kernel's completion (a no-op after an ordinary launch).
-  grid_dependency_wait();
 
   // ---- this warp's view of x: the strip's values for the MMA's B operand. Lanes of column g
   // hold hidden row g (zeros for g >= mt); with one hidden row every lane holds it.

@@ -246,8 +246,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
   int issued = 0, issued_b = 0;  // copies issued by warp 0 / warp 2 (lane 0)
   if (warp == 0) {
-    // ---- packed rows: ring stages in order (weights: no wait on the preceding kernel) ---------
+    // ---- packed rows: ring stages in order. The first stages go to L2 while the preceding
+    // kernel may still run (it may have written the weights: only L2, which is coherent, is
+    // touched before griddepcontrol.wait); every copy into shared memory comes after the wait.
     if (lane == 0) {
+      for (int s = 0; s < np && s < total_stages; ++s)
+        tma_prefetch_l2_2d(&tmap, (s % a.NS) * kWStageBytes, tile_of(s / a.NS) * kWRows);
+      grid_dependency_wait();
       for (; issued < total_stages; ++issued) {
         const int slot = issued % np;
         if (issued >= np) wait_bar(&pempty[slot], static_cast<uint32_t>(issued / np - 1) & 1u);
@@ -373,8 +378,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       uint32_t* keys = reinterpret_cast<uint32_t*>(sm + a.off_keys);  // [128][PITCH]
       float* xsd = reinterpret_cast<float*>(sm + a.off_xs);           // [KG][NCOL]
       int* ew_s = reinterpret_cast<int*>(sm + a.off_ew);              // [NCOL]
-      // the half-0 warp copies the row's S, the half-1 warp its ZS (weights' scales: no wait on
-      // the preceding kernel); a barrier of the fold warps then shares them
+      // the half-0 warp copies the row's S, the half-1 warp its ZS; a barrier of the fold warps
+      // then shares them
       auto load_sz = [&](int lt) {
         const int n = tile_of(lt) * kWRows + row;
         const bool valid = n < a.N;
@@ -384,11 +389,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
         for (int i = 0; i < a.KG / 8; ++i) w_cp_async16(smem_addr(dst + 16 * i), src + 8 * i, valid);
         asm volatile("cp.async.commit_group;" ::: "memory");
       };
-      if (my_tiles > 0) load_sz(0);
+      // the first tile's scales into L2 while the preceding kernel may still run (only L2
+      // before the wait, as for the packed rows); the copies into shared memory follow it
+      if (my_tiles > 0) {
+        const int n = tile_of(0) * kWRows + row;
+        if (n < a.N)
+          prefetch_l2_bulk((half ? a.ZS : a.S) + static_cast<int64_t>(n) * a.KG,
+                           static_cast<uint32_t>(a.KG * 2));
+      }
       // the prep kernel's group sums and exponents (the outputs are written after this wait
       // too): XS in the units of the D slots, 2^24 / (2^(15 - E_m) 4) = 2^(E_m + 7), as
       // xsd[g][m] = XS[m][g] 2^-(E_m + 7) (a power of two: exact)
       grid_dependency_wait();
+      if (my_tiles > 0) load_sz(0);
       const int ftid = fw * 32 + lane;
       if (ftid < NCOL) ew_s[ftid] = a.ew[ftid];
       for (int i = ftid; i < NCOL * a.KG; i += 256) {

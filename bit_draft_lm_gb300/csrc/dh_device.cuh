@@ -115,6 +115,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Warm the L2 cache with global memory, without touching this SM's L1 or shared memory. Safe
+// before griddepcontrol.wait on data that the preceding kernel may still be writing: L2 is the
+// device's point of coherence, so a later write of the preceding kernel updates the line, and
+// everything read after the wait sees it. Bulk form: p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // Orders this thread's earlier shared-memory accesses before later async-proxy (bulk copy)
 // accesses to shared memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

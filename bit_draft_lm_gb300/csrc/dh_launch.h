@@ -72,5 +72,11 @@ cudaError_t launch_topk_only(const int32_t* rr_id, const float* rr_logit, int64_
 int record_error(int code, const char* msg);
 // Workspace bytes dh_draft_head_rerank_argmax requires (independent of the sizes).
 size_t rerank_workspace_needed();
+// dh_draft_head_rerank_argmax's argument checks (api.cu): DH_OK, or the failing check's status
+// with its dh_last_error() message recorded.
+int check_rerank_call(const char* who, const void* x, int64_t M, int64_t K, const void* W,
+                      int64_t N, const float* cand_val, const int32_t* cand_id, int64_t ncand,
+                      int rerank, int32_t* rr_id, float* rr_logit, int32_t* argmax_id,
+                      void* y_coarse);
 
 }  // namespace dh

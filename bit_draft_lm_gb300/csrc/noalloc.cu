@@ -56,31 +56,29 @@ extern "C" int dh_draft_head_rerank_argmax_noalloc(const void* x, int64_t M, int
                                                    int rerank, int32_t* rr_id, float* rr_logit,
                                                    int32_t* argmax_id, void* y_coarse,
                                                    dh_stream_t s) {
-  const size_t need = M < 1 ? 0 : dh::rerank_workspace_needed();
-  if (need == 0) {
-    char msg[160];
-    snprintf(msg, sizeof msg, "draft_head_rerank_argmax_noalloc: M=%lld out of range",
-             static_cast<long long>(M));
-    return dh::record_error(DH_ERR_SHAPE, msg);
-  }
-  if (need > DH_NOALLOC_SCRATCH_BYTES) {
-    char msg[256];
-    snprintf(msg, sizeof msg,
-             "draft_head_rerank_argmax_noalloc: these sizes (M=%lld, rerank=%d) need %zu bytes "
-             "of workspace, more than the fixed %u-byte scratch; call "
-             "dh_draft_head_rerank_argmax with a workspace instead",
-             static_cast<long long>(M), rerank, need, DH_NOALLOC_SCRATCH_BYTES);
+  const char* who = "draft_head_rerank_argmax_noalloc";
+  // Every argument is checked first, with the checks of dh_draft_head_rerank_argmax (sizes out
+  // of range: DH_ERR_SHAPE with a message), so that a refused call leaves nothing on the stream.
+  int rc = dh::check_rerank_call(who, x, M, K, W, N, cand_val, cand_id, ncand, rerank, rr_id,
+                                 rr_logit, argmax_id, y_coarse);
+  if (rc != DH_OK) return rc;
+  // The rerank's workspace is its status header, the same for every accepted size, so every
+  // call the checks above accept fits in the array.
+  const size_t need = dh::rerank_workspace_needed();
+  if (need > DH_NOALLOC_SCRATCH_BYTES) {  // not reachable with the library's sizes
+    char msg[200];
+    snprintf(msg, sizeof msg, "%s: %zu bytes of workspace needed, more than the fixed %u-byte "
+             "scratch", who, need, DH_NOALLOC_SCRATCH_BYTES);
     return dh::record_error(DH_ERR_SHAPE, msg);
   }
   void* ws = nullptr;
-  int rc = scratch_address(&ws);
+  rc = scratch_address(&ws);
   if (rc != DH_OK) return rc;
   // The array keeps the previous call's contents (status word included): start from zero.
   cudaError_t e = cudaMemsetAsync(ws, 0, need, reinterpret_cast<cudaStream_t>(s));
   if (e != cudaSuccess) {
     char msg[256];
-    snprintf(msg, sizeof msg, "draft_head_rerank_argmax_noalloc: clearing the scratch: %s",
-             cudaGetErrorString(e));
+    snprintf(msg, sizeof msg, "%s: clearing the scratch: %s", who, cudaGetErrorString(e));
     return dh::record_error(DH_ERR_CUDA, msg);
   }
   return dh_draft_head_rerank_argmax(x, M, K, W, N, cand_val, cand_id, ncand, rerank, rr_id,

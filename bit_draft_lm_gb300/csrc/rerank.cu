@@ -449,14 +449,13 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
   // on the SMs this small grid leaves idle; it waits for this grid before reading anything else
   if (tid == 0) grid_launch_dependents();
 
-  // 1. x for the dots (an input of the call, not of the previous kernel: staged before the
-  // wait), then, once the kernel that wrote the candidates has completed (programmatic
-  // dependent launch; a no-op otherwise), the keys and ids of this CTA's slots
-  {
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
-    for (int i = tid; i < a.K / 8; i += kRCThreads) reinterpret_cast<uint4*>(xs)[i] = xr[i];
-  }
+  // 1. once the preceding kernel has completed and its writes are visible (programmatic
+  // dependent launch; a no-op otherwise): x for the dots (it may be that kernel's output),
+  // then the keys and ids of this CTA's slots. Before the wait, x is only fetched into L2.
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
+  if (tid < a.K / 64) prefetch_l2(xr + 8 * tid);
   grid_dependency_wait();
+  for (int i = tid; i < a.K / 8; i += kRCThreads) reinterpret_cast<uint4*>(xs)[i] = xr[i];
   uint32_t key[LPT], uid[LPT];
 #pragma unroll
   for (int j = 0; j < LPT; ++j) {

@@ -116,10 +116,11 @@ size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank
  *   workspace device buffer of ws_bytes >= dh_workspace_bytes(M, N, K, ...), 256-B aligned.
  * Up to 16 hidden rows (and every int4 call) run on warp-level MMAs in passes of 8 rows; more
  * than 16 rows of an int2 head run on the 5th-generation tensor cores in passes of up to 80.
- * The kernels are launched as programmatic dependents: they read the weights (packed, S, ZS)
- * before the preceding kernel in the stream has completed if that kernel lets its dependents
- * start early (this library's rerank does), and x and every output only after it. So the
- * weights must not be written by such a kernel directly before this call.
+ * The kernels are launched as programmatic dependents: while the preceding kernel in the stream
+ * finishes (if it lets its dependents start early, as this library's rerank does) they only warm
+ * the L2 cache with the first weight tiles; every read of an input into the SMs, and every
+ * output write, happens after that kernel has completed and its writes are visible. So any
+ * kernel may produce x, packed, S or ZS directly before this call.
  */
 int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
                               const void* S, const void* ZS, int64_t N, int G, int bits,
@@ -172,14 +173,16 @@ int dh_draft_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* pac
  * workspace that dh_draft_head_rerank_argmax takes.
  *   Arguments, outputs and results are those of dh_draft_head_rerank_argmax (same kernels).
  *   Workspace: a fixed array of DH_NOALLOC_SCRATCH_BYTES among the library's device globals;
- *     every device that loads the library holds it until the process exits. Sizes whose
- *     workspace (dh_workspace_bytes(M, N, K, 1, rerank)) exceeds it are rejected with
- *     DH_ERR_SHAPE and a message; use dh_draft_head_rerank_argmax for those.
+ *     every device that loads the library holds it until the process exits. The rerank's
+ *     workspace is the 256-byte status header whatever the sizes, so every call that passes
+ *     the argument checks fits; sizes out of range (M > DH_MAX_TOKENS, K > 32768, ncand > 2^20,
+ *     rerank > DH_MAX_RERANK, ...) are rejected with DH_ERR_SHAPE or DH_ERR_PARAM and a
+ *     message, before anything is enqueued, by the checks of dh_draft_head_rerank_argmax.
  *   Set-up: the first call on a device, with that device current, looks up the array's device
  *     address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
  *     capture on that device.
- *   Each call clears the part of the array it uses (cudaMemsetAsync on s) and then launches;
- *     nothing is allocated or freed.
+ *   Each call that passes the checks clears the part of the array it uses (cudaMemsetAsync on
+ *     s) and then launches; nothing is allocated or freed.
  *   All calls on a device share the one array and it keeps the last call's contents: calls
  *     that overlap on the GPU (different streams without ordering between them) race on it and
  *     give wrong results. Order them on one stream.
