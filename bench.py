@@ -281,10 +281,35 @@ def run_ours(args, rank, world):
                          "steps": steps}
     # the page's two ablations at M=8 (the comparison workload): the 4-bit head with KCAND=1, and
     # the int2 head with 64-wide groups
+    # recall on the golden rows (written by the oracle alone; tests/golden/make_recall.py): the
+    # timed kernels, in 8-row calls, against the brute-force exact argmax of every row
+    gold = recall_golden()
+
+    def recall(name, bits, group, kcand, pk):
+        if gold is None or name not in gold["configs"]:
+            return None
+        from bit_draft_lm_gb300 import synth
+        cfg = gold["configs"][name]
+        xr = torch.from_numpy(synth.recall_rows(synth.named(gold["head"])).view(np.int16))
+        xr = xr.to(dev).view(torch.bfloat16)
+        am = []
+        for m0 in range(0, xr.shape[0], 8):
+            am.append(dh.dh_draft_head_argmax(xr[m0:m0 + 8], pk[0], pk[1], pk[2], Ws[0], group,
+                                              bits, kcand, cfg["rerank"])[2])
+        am = torch.cat(am).cpu().numpy()
+        ex, method = np.asarray(gold["exact_argmax"]), np.asarray(cfg["method_argmax"])
+        miss = np.nonzero(am != ex)[0].tolist()
+        return {"rows": int(ex.size), "misses": len(miss), "miss_rows": miss,
+                "oracle_method_misses": len(cfg["misses"]),
+                "same_argmax_as_oracle_method": int((am == method).sum()),
+                "rerank": cfg["rerank"], "kcand": kcand}
+
+    headline_recall = recall("int2_g128_kcand8", 2, GROUP, KCAND, packs[0])
     variants = {}
     if not args.no_variants:
-        for name, bits, group, kc, per in (("int4_g128_m8_kcand1", 4, 128, 1, 2),
-                                           ("int2_g64_m8_kcand8", 2, 64, KCAND, 4)):
+        for name, gname, bits, group, kc in (
+                ("int4_g128_m8_kcand1", "int4_g128_kcand1", 4, 128, 1),
+                ("int2_g64_m8_kcand8", "int2_g64_kcand8", 2, 64, KCAND)):
             quant = dh.dh_quantize_pack_int4 if bits == 4 else dh.dh_quantize_pack_int2
             vp = [quant(Wc, group) for Wc in Ws]
             steps = max(50, min(args.steps, 1000))
@@ -293,7 +318,8 @@ def run_ours(args, rank, world):
             alg = dh.dh_packed_bytes(N_VOCAB, K_DIM, group, bits) + 8 * RERANK * K_DIM * 2
             variants[name] = {"us_per_call": round(u, 3), "coarse_us": round(1e3 * cm / steps, 3),
                               "algorithmic_bytes_per_call": alg,
-                              "hbm_gbs_per_call": round(alg / u / 1e3, 1), "steps": steps}
+                              "hbm_gbs_per_call": round(alg / u / 1e3, 1), "steps": steps,
+                              "recall": recall(gname, bits, group, kc, vp[0])}
             del vp
             torch.cuda.synchronize()
         # the FP8 checkpoint's head at M=1: int2 codes quantised from e4m3 rows x row scale, the
@@ -355,12 +381,22 @@ def run_ours(args, rank, world):
         "clocks": dict(clk, window=f"timed region + {soak_t:.1f} s of the same step"),
         "per_m": extra,
         "variants": variants,
+        "recall": headline_recall,
     }
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline and rank == 0:
         line["cpu_baseline"] = cpu_baseline(args.m, budget_s=15.0)
     return line
+
+
+def recall_golden():
+    """The recall report's stored rows and expected ids (None if the file is absent)."""
+    try:
+        with open(os.path.join(ROOT, "tests", "golden", "recall_k5120_n124160_m64.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
 
 
 def extra_ms(args):
@@ -370,8 +406,8 @@ def extra_ms(args):
 def run_e2e(args, dev, Ws, xs_h, ncopy):
     """The C-ABI call with host buffers (DraftHead.call_host: a dh_host_plan run every step, which
     takes x from pinned host memory, runs the head, puts argmax / rr_id / rr_logit into pinned
-    host memory and synchronises). dh_draft_head_host with all its arguments and the
-    graph-replayed DraftHead.infer are timed beside it."""
+    host memory and synchronises). dh_draft_head_host with all its arguments is timed beside
+    it."""
     import torch
     from bit_draft_lm_gb300 import drafthead as dh
     M = args.m
@@ -391,21 +427,20 @@ def run_e2e(args, dev, Ws, xs_h, ncopy):
 
     v = timed(lambda h, x: h.call_host(x))
     d = timed(lambda h, x: h.call_host(x, plan=False))
-    g = timed(lambda h, x: h.infer(x))
     for h in heads:
         if dh.dh_workspace_status(h.workspace):
             raise RuntimeError("kernel status word set in the end-to-end run")
     return {"value": round(v, 3), "unit": "us/call", "h2d_bytes_per_step": M * K_DIM * 2,
             "d2h_bytes_per_step": M * 4 + 2 * M * RERANK * 4, "steps": steps,
             "api": "dh_host_plan_run (C ABI, host buffers; plan prepared once per M)",
-            "direct_call_value": round(d, 3),
-            "graph_replay_value": round(g, 3)}
+            "direct_call_value": round(d, 3)}
 
 
 # ------------------------------------------------------------------------------------ oracle arm
-def oracle_sample(M, rows):
-    """Quantise a slice of the head with the oracle (untimed) and return a callable running the
-    oracle's full path (coarse -> block top-K -> top-R -> rerank -> argmax) on that slice."""
+def oracle_sample(M, rows, nthreads=None):
+    """Quantise a slice of the head with the oracle (untimed) and return callables running the
+    oracle's full path (coarse -> block top-K -> top-R -> rerank -> argmax) and its quantiser
+    (a0) on that slice."""
     import oracle
     xs_h, W_h = workload_host(M)
     Ws = np.ascontiguousarray(W_h[:rows])
@@ -413,43 +448,65 @@ def oracle_sample(M, rows):
     packed, S, ZS = oracle.quantize_pack(Ws, GROUP, 2)
 
     def call():
-        return oracle.head(x, packed, S, ZS, Ws, G=GROUP, bits=2, kcand=KCAND, R=RERANK)
-    return call
+        return oracle.head(x, packed, S, ZS, Ws, G=GROUP, bits=2, kcand=KCAND, R=RERANK,
+                           nthreads=nthreads)
+
+    def quant():
+        return oracle.quantize_pack(Ws, GROUP, 2, nthreads=nthreads)
+    return call, quant
+
+
+def _median_time(fn, budget_s, at_least=3, at_most=50):
+    fn()
+    times = []
+    t_start = time.perf_counter()
+    while (time.perf_counter() - t_start < budget_s or len(times) < at_least) and \
+            len(times) < at_most:
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times), len(times)
 
 
 def cpu_baseline(M, budget_s):
-    """The oracle as it stands, on the host cores, on a bounded slice of the same head; time per
-    call scaled to the full vocabulary (the slice's rows are a fixed fraction of N)."""
+    """The oracle as it stands, on the host cores, on bounded slices of the same head; times per
+    call scaled to the full vocabulary (each slice's rows are a fixed fraction of N). The
+    all-core figure is the line's value; beside it the single-thread figure and the quantiser
+    (a0, load time, not part of a call), each a median of at least 3 runs."""
     import oracle
     rows = 15520                                # 1/8 of the vocabulary, whole 64-row blocks
-    call = oracle_sample(M, rows)
-    call()
-    times = []
-    t_start = time.perf_counter()
-    while time.perf_counter() - t_start < budget_s or len(times) < 3:
-        t0 = time.perf_counter()
-        call()
-        times.append(time.perf_counter() - t0)
-        if len(times) >= 50:
-            break
-    scale = N_VOCAB / rows
-    return {"value": round(statistics.median(times) * scale * 1e6, 1), "unit": "us/call",
+    call, quant = oracle_sample(M, rows)
+    t_all, n_all = _median_time(call, budget_s)
+    t_q, n_q = _median_time(quant, 0.2 * budget_s)
+    rows1 = 1940                                # 1/64 of the vocabulary, on one thread
+    call1, _ = oracle_sample(M, rows1, nthreads=1)
+    t_1, n_1 = _median_time(call1, 0.2 * budget_s)
+    scale, scale1 = N_VOCAB / rows, N_VOCAB / rows1
+    return {"value": round(t_all * scale * 1e6, 1), "unit": "us/call",
             "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{len(times)} calls of the oracle's full path on a {rows}-row slice "
-                      f"(1/{int(scale)}) of the N={N_VOCAB} head at M={M}, median x {scale:g}"}
+            "sample": f"median of {n_all} calls of the oracle's full path on a {rows}-row slice "
+                      f"(1/{int(scale)}) of the N={N_VOCAB} head at M={M}, x {scale:g}",
+            "single_thread": {"value": round(t_1 * scale1 * 1e6, 1), "unit": "us/call",
+                              "cores": 1,
+                              "sample": f"median of {n_1} calls on a {rows1}-row slice, "
+                                        f"x {scale1:g}"},
+            "quantize_a0": {"value": round(t_q * scale * 1e3, 2), "unit": "ms/head",
+                            "cores": oracle.threads(),
+                            "sample": f"median of {n_q} oracle quantise + pack runs of the "
+                                      f"{rows}-row slice, x {scale:g} (load time: not in a call)"}}
 
 
 def run_reference(args):
     """--impl reference: the CPU oracle timed per step on a bounded slice of the workload."""
     import oracle
-    probe = oracle_sample(args.m, 1940)
+    probe, _ = oracle_sample(args.m, 1940)
     t0 = time.perf_counter()
     probe()
     t_small = max(time.perf_counter() - t0, 1e-4)
     per_step_budget = 120.0 / max(args.steps + args.warmup, 1)
     rows = int(1940 * per_step_budget / t_small) // 64 * 64
     rows = max(128, min(rows, N_VOCAB // 4))
-    call = probe if rows == 1940 else oracle_sample(args.m, rows)
+    call = probe if rows == 1940 else oracle_sample(args.m, rows)[0]
     for _ in range(args.warmup):
         call()
     times = []

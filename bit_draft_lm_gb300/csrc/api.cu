@@ -403,6 +403,71 @@ int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, 
 
 }  // extern "C"
 
+// ---- vocabulary-sharded argmax merge -------------------------------------------------------------
+static int check_shard_keys(const char* who, const int32_t* rr_id, const float* rr_logit,
+                            int64_t M, int rerank, int64_t id_offset, const int64_t* keys) {
+  if (!rr_id || !rr_logit || !keys) return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  if (M < 1 || M > DH_MAX_TOKENS || rerank < 1 || rerank > DH_MAX_RERANK)
+    return fail(DH_ERR_SHAPE, "%s: M=%lld rerank=%d", who, (long long)M, rerank);
+  if (id_offset < 0 || id_offset > (int64_t)INT32_MAX)
+    return fail(DH_ERR_SHAPE, "%s: id_offset=%lld (0..2^31-1)", who, (long long)id_offset);
+  if (!aligned(rr_id, 4) || !aligned(rr_logit, 4) || !aligned(keys, 8))
+    return fail(DH_ERR_ALIGN, "%s: misaligned array", who);
+  return DH_OK;
+}
+
+static int check_merge(const char* who, const int64_t* keys, int P, int64_t M,
+                       const int32_t* argmax_id, const float* logit) {
+  if (!keys || !argmax_id) return fail(DH_ERR_NULL, "%s: NULL pointer", who);
+  if (P < 1 || P > 65536 || M < 1 || M > DH_MAX_TOKENS)
+    return fail(DH_ERR_SHAPE, "%s: P=%d M=%lld", who, P, (long long)M);
+  if (!aligned(keys, 8) || !aligned(argmax_id, 4) || (logit && !aligned(logit, 4)))
+    return fail(DH_ERR_ALIGN, "%s: misaligned array", who);
+  return DH_OK;
+}
+
+extern "C" {
+
+int dh_argmax_shard_keys(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
+                         int64_t id_offset, int64_t* keys, dh_stream_t s) {
+  const char* who = "argmax_shard_keys";
+  int rc = check_shard_keys(who, rr_id, rr_logit, M, rerank, id_offset, keys);
+  if (rc != DH_OK) return rc;
+  cudaError_t e = dh::launch_shard_keys(rr_id, rr_logit, M, rerank, id_offset, keys,
+                                        reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "argmax_shard_keys launch");
+  return ok();
+}
+
+int dh_argmax_merge(const int64_t* keys, int P, int64_t M, int32_t* argmax_id, float* logit,
+                    dh_stream_t s) {
+  const char* who = "argmax_merge";
+  int rc = check_merge(who, keys, P, M, argmax_id, logit);
+  if (rc != DH_OK) return rc;
+  cudaError_t e =
+      dh::launch_merge_keys(keys, P, M, argmax_id, logit, reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "argmax_merge launch");
+  return ok();
+}
+
+int dh_argmax_shard_keys_host(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
+                              int64_t id_offset, int64_t* keys) {
+  int rc = check_shard_keys("argmax_shard_keys_host", rr_id, rr_logit, M, rerank, id_offset, keys);
+  if (rc != DH_OK) return rc;
+  dh::shard_keys_host(rr_id, rr_logit, M, rerank, id_offset, keys);
+  return ok();
+}
+
+int dh_argmax_merge_host(const int64_t* keys, int P, int64_t M, int32_t* argmax_id,
+                         float* logit) {
+  int rc = check_merge("argmax_merge_host", keys, P, M, argmax_id, logit);
+  if (rc != DH_OK) return rc;
+  dh::merge_keys_host(keys, P, M, argmax_id, logit);
+  return ok();
+}
+
+}  // extern "C"
+
 // Checks of the host-memory call's own arguments (the device calls it makes check the rest).
 static int check_host(const char* who, const void* x_host, int64_t M, int64_t K, void* x_dev,
                       int rerank, int32_t* argmax_host, int32_t* rr_id_host,

@@ -68,6 +68,16 @@ cudaError_t launch_stage_in(const void* src, void* dst, size_t bytes, cudaStream
 // y [M, N] bf16 = -inf except y[m, rr_id[m, j]] = bf16(rr_logit[m, j]) (topk_only.cu).
 cudaError_t launch_topk_only(const int32_t* rr_id, const float* rr_logit, int64_t M, int R,
                              int64_t N, void* y, cudaStream_t s);
+// Vocabulary-sharded argmax merge (shard_merge.cu): per-row int64 keys of a shard's reranked
+// lists, and their merge over P shards ([P, M] keys) into global argmax ids and logits; device
+// kernels and the same arithmetic on host arrays.
+cudaError_t launch_shard_keys(const int32_t* rr_id, const float* rr_logit, int64_t M, int R,
+                              int64_t id_offset, int64_t* keys, cudaStream_t s);
+cudaError_t launch_merge_keys(const int64_t* keys, int P, int64_t M, int32_t* argmax_id,
+                              float* logit, cudaStream_t s);
+void shard_keys_host(const int32_t* rr_id, const float* rr_logit, int64_t M, int R,
+                     int64_t id_offset, int64_t* keys);
+void merge_keys_host(const int64_t* keys, int P, int64_t M, int32_t* argmax_id, float* logit);
 // Sets the calling thread's dh_last_error() message; returns `code`.
 int record_error(int code, const char* msg);
 // Workspace bytes dh_draft_head_rerank_argmax requires (independent of the sizes).

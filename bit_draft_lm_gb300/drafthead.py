@@ -57,6 +57,10 @@ SIGNATURES = {
     "dh_quantize_pack_int2_fp8": ([_P, _P, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "dh_draft_head_rerank_argmax_fp8": ([_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _I, _P, _P,
                                          _P, _P, _P, _SZ, _P], _I),
+    "dh_argmax_shard_keys": ([_P, _P, _I64, _I, _I64, _P, _P], _I),
+    "dh_argmax_merge": ([_P, _I, _I64, _P, _P, _P], _I),
+    "dh_argmax_shard_keys_host": ([_P, _P, _I64, _I, _I64, _P], _I),
+    "dh_argmax_merge_host": ([_P, _I, _I64, _P, _P], _I),
     "dh_workspace_status": ([_P, _SZ, _P, _P], _I),
     "dh_last_error": ([], ctypes.c_char_p),
 }
@@ -367,6 +371,78 @@ def dh_topk_only_logits(rr_id: torch.Tensor, rr_logit: torch.Tensor, N: int, y=N
     return y
 
 
+def _host(t: Optional[torch.Tensor], name: str, dtype, shape=None) -> int:
+    if t is None:
+        return 0
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def vocab_shard(N: int, world: int, rank: int) -> Tuple[int, int]:
+    """Vocab rows [n0, n1) of `rank`'s shard: the ceil(N/64) candidate blocks split as evenly as
+    possible in rank order, so that no 64-row block straddles two shards."""
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    b0, b1 = rank * nblk // world, (rank + 1) * nblk // world
+    return min(N, BLOCK_ROWS * b0), min(N, BLOCK_ROWS * b1)
+
+
+def dh_argmax_shard_keys(rr_id: torch.Tensor, rr_logit: torch.Tensor, id_offset: int,
+                         keys=None, stream=None) -> torch.Tensor:
+    """int64 [M] keys of a shard's reranked lists (rr_id shard-local, id_offset = the shard's first
+    vocab row): the largest key over all shards names the global argmax. Device tensors run the
+    library's kernel on the stream; host tensors its host routine."""
+    M, R = rr_id.shape
+    if keys is None:
+        keys = torch.empty(M, dtype=torch.int64, device=rr_id.device)
+    if rr_id.is_cuda:
+        _check(lib().dh_argmax_shard_keys(_dev(rr_id, "rr_id", torch.int32, (M, R)),
+                                          _dev(rr_logit, "rr_logit", torch.float32, (M, R)), M, R,
+                                          id_offset, _dev(keys, "keys", torch.int64, (M,)),
+                                          _stream(stream)))
+    else:
+        _check(lib().dh_argmax_shard_keys_host(_host(rr_id, "rr_id", torch.int32, (M, R)),
+                                               _host(rr_logit, "rr_logit", torch.float32, (M, R)),
+                                               M, R, id_offset,
+                                               _host(keys, "keys", torch.int64, (M,))))
+    return keys
+
+
+def dh_argmax_merge(keys: torch.Tensor, argmax_id=None, logit=None, stream=None):
+    """keys int64 [P, M] (P shards' keys, or [1, M] after a MAX all-reduce) -> (argmax_id int32 [M],
+    logit float32 [M]): the global argmax vocab id and its reranked logit."""
+    P, M = keys.shape
+    dev = keys.device
+    if argmax_id is None:
+        argmax_id = torch.empty(M, dtype=torch.int32, device=dev)
+    if logit is None:
+        logit = torch.empty(M, dtype=torch.float32, device=dev)
+    if keys.is_cuda:
+        _check(lib().dh_argmax_merge(_dev(keys, "keys", torch.int64, (P, M)), P, M,
+                                     _dev(argmax_id, "argmax_id", torch.int32, (M,)),
+                                     _dev(logit, "logit", torch.float32, (M,)), _stream(stream)))
+    else:
+        _check(lib().dh_argmax_merge_host(_host(keys, "keys", torch.int64, (P, M)), P, M,
+                                          _host(argmax_id, "argmax_id", torch.int32, (M,)),
+                                          _host(logit, "logit", torch.float32, (M,))))
+    return argmax_id, logit
+
+
+def merge_argmax_across_ranks(rr_id: torch.Tensor, rr_logit: torch.Tensor, id_offset: int,
+                              group=None):
+    """The exchange of the vocabulary-sharded head: this rank's keys, one MAX all-reduce over the
+    process group (NCCL for device tensors, gloo for host tensors), then the decode. Returns
+    (argmax_id [M] global vocab ids, logit [M]), the same on every rank."""
+    import torch.distributed as dist
+    keys = dh_argmax_shard_keys(rr_id, rr_logit, id_offset)
+    dist.all_reduce(keys, op=dist.ReduceOp.MAX, group=group)
+    return dh_argmax_merge(keys.view(1, -1))
+
+
 def dh_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the workspace status word (0 = no kernel failure)."""
     word = ctypes.c_uint32(0)
@@ -401,27 +477,20 @@ class DraftHead:
         self._am = torch.empty(max_tokens, dtype=torch.int32, device=dev)
 
     def infer(self, x_host: torch.Tensor, stream=None):
-        """End-to-end call from host memory: copies x_host (bf16 [M, K]) to the device, runs the
-        head, copies argmax [M], rr_id [M, R] and rr_logit [M, R] back to pinned host memory and
-        synchronises the stream. Returns those host tensors (views of a buffer the next call
-        with the same M overwrites).
-
-        The step is one CUDA graph per M, captured on the first call: the copy in (from a
-        pinned staging buffer that x_host is copied into on the host), dh_draft_head_argmax
-        (the coarse and rerank kernels) and one copy out of the three results, which sit in one
-        device buffer."""
+        """End-to-end call from any host tensor: x_host (bf16 [M, K], pageable or pinned) is
+        copied into this head's pinned staging buffer, then the call runs through call_host (the
+        library's host-memory plan: copy in, coarse pass, rerank, results out and the
+        synchronisation, all native). Returns pinned host tensors argmax [M], rr_id [M, R] and
+        rr_logit [M, R], views of buffers the next call with the same M overwrites."""
         M = x_host.shape[0]
         if M < 1 or M > self.max_tokens:
             raise ValueError(f"M={M} outside 1..max_tokens={self.max_tokens}")
-        g = self._infer_graphs.get(M) if hasattr(self, "_infer_graphs") else None
-        if g is None:
-            g = self._build_infer_graph(M)
-        s = stream if stream is not None else torch.cuda.current_stream()
-        g["h_x"].copy_(_bf16(x_host, "x_host"))
-        with torch.cuda.stream(s):
-            g["graph"].replay()
-        s.synchronize()
-        return g["h_am"], g["h_rr"], g["h_rl"]
+        if getattr(self, "_stage", None) is None:
+            self._stage = torch.empty(self.max_tokens, self.K, dtype=torch.bfloat16,
+                                      pin_memory=True)
+        st = self._stage[:M]
+        st.copy_(_bf16(x_host, "x_host"))
+        return self.call_host(st, stream)
 
     def call_host(self, x_host: torch.Tensor, stream=None, plan: bool = True):
         """The same end-to-end call through the library's host-memory entry points: copy in,
@@ -479,41 +548,6 @@ class DraftHead:
                 except Exception:
                     pass
             calls.clear()
-
-    def _build_infer_graph(self, M: int) -> dict:
-        dev, R = self.W.device, self.rerank
-        g = {"h_x": torch.empty(M, self.K, dtype=torch.bfloat16, pin_memory=True),
-             "d_x": torch.empty(M, self.K, dtype=torch.bfloat16, device=dev),
-             "d_out": torch.empty(M * (1 + 2 * R), dtype=torch.int32, device=dev),
-             "h_out": torch.empty(M * (1 + 2 * R), dtype=torch.int32, pin_memory=True)}
-        d_am = g["d_out"][:M]
-        d_rr = g["d_out"][M:M + M * R].view(M, R)
-        d_rl = g["d_out"][M + M * R:].view(torch.float32).view(M, R)
-        g["h_am"] = g["h_out"][:M]
-        g["h_rr"] = g["h_out"][M:M + M * R].view(M, R)
-        g["h_rl"] = g["h_out"][M + M * R:].view(torch.float32).view(M, R)
-
-        def step():
-            g["d_x"].copy_(g["h_x"], non_blocking=True)
-            dh_draft_head_argmax(g["d_x"], self.packed, self.S, self.ZS, self.W, self.G,
-                                 self.bits, self.kcand, R, cand_val=self._cv[:M],
-                                 cand_id=self._ci[:M], rr_id=d_rr, rr_logit=d_rl,
-                                 argmax_id=d_am, workspace=self.workspace)
-            g["h_out"].copy_(g["d_out"], non_blocking=True)
-
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            step()  # once outside the capture: first-call set-up of the library
-        side.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=side):
-            step()
-        g["graph"] = graph
-        if not hasattr(self, "_infer_graphs"):
-            self._infer_graphs = {}
-        self._infer_graphs[M] = g
-        return g
 
     def __call__(self, x: torch.Tensor, y_coarse=None, stream=None):
         """x bf16 [M, K] on the device -> dict of argmax [M], rr_id [M, R], rr_logit [M, R],

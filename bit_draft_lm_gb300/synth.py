@@ -175,6 +175,47 @@ def named(name: str) -> Workload:
     return _CACHE[name]
 
 
+def hidden_rows(M: int, K: int, seed: int, rms_norm: bool = True) -> np.ndarray:
+    """M fresh hidden rows (bf16 bits [M, K]) by the recipe above: z ~ N(0, 1), RMS-normalised
+    unless ``rms_norm`` is False. Used with a cached head to draw more rows without redrawing W."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((M, K))
+    if rms_norm:
+        z = z / np.sqrt(np.mean(z * z, axis=1, keepdims=True))
+    return bf16_bits(z)
+
+
+RECALL_HEAD = "head_m1_k5120_n124160"
+RECALL_ROWS, RECALL_SEED = 64, 7
+
+
+def recall_rows(w: Workload) -> np.ndarray:
+    """The hidden rows of the recall report on head ``w``: its own row 0 (the planted rows and
+    near-tie pairs face it), then RECALL_ROWS - 1 fresh rows of seed RECALL_SEED."""
+    x = hidden_rows(RECALL_ROWS, w.K, RECALL_SEED)
+    x[0] = w.x[0]
+    return x
+
+
+def wide_range_rows(M: int, K: int, seed: int) -> np.ndarray:
+    """Hidden rows with an extreme dynamic range (bf16 bits [M, K]), to exercise the kernels'
+    per-row power-of-two scaling of x: row 0 is 2^-20 z with two spikes of +-2^12; row 1 is
+    2^-20 z alone (a tiny maximum); row 2 mixes 2^-20 z and z halves (a spike-free wide range);
+    further rows are plain RMS-normalised draws."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((M, K))
+    z = z / np.sqrt(np.mean(z * z, axis=1, keepdims=True))
+    if M > 0:
+        z[0] *= 2.0 ** -20
+        i, j = rng.choice(K, 2, replace=False)
+        z[0, i], z[0, j] = 2.0 ** 12, -(2.0 ** 12)
+    if M > 1:
+        z[1] *= 2.0 ** -20
+    if M > 2:
+        z[2, : K // 2] *= 2.0 ** -20
+    return bf16_bits(z)
+
+
 def fp8_head(W: np.ndarray):
     """An FP8 per-channel head built from a bf16 head (bit patterns uint16 [N, K]): the fp32
     row scale max|W[n]| / 448 and the e4m3 bytes of W / scale (round to nearest even, the

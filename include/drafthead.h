@@ -219,6 +219,34 @@ int dh_topk_only_logits(const int32_t* rr_id, const float* rr_logit, int64_t M, 
                         int64_t N, void* y, dh_stream_t s);
 
 /*
+ * Vocabulary-sharded argmax merge (the page's head is "per rank" one vocab shard of the lm_head:
+ * module docstring, and the launch-geometry notes timing one rank's 124160-row shard). The vocab
+ * rows are split across ranks at multiples of DH_BLOCK_ROWS, so no candidate block straddles two
+ * shards; each rank runs the path on its rows (packed, S, ZS and W are row slices; candidate and
+ * rr ids are shard-local) and the ranks exchange one 64-bit key per hidden row:
+ *   key = (order-preserving bits of the logit) << 32 | (0xFFFFFFFF - global id), top bit flipped,
+ * so that the largest signed key over all shards is the global argmax, equal logits going to the
+ * lowest vocab id, and a MAX all-reduce of int64 (NCCL or gloo) is the whole exchange.
+ *
+ * dh_argmax_shard_keys: keys [M] int64 out = the key of the best (logit, id + id_offset) among
+ *   the rerank slots of each row (rr_id, rr_logit [M, rerank] as written by the rerank; slots with
+ *   an id < 0 are skipped; a row with none gets INT64_MIN). id_offset: the shard's first vocab
+ *   row, 0 .. 2^31 - 1. Device arrays, asynchronous on s.
+ * dh_argmax_merge: keys [P, M] int64 (P shards' keys, e.g. gathered; P = 1 for keys a MAX
+ *   all-reduce already combined) -> argmax_id [M] (global vocab id, -1 if no candidate) and, if
+ *   logit is not NULL, logit [M] (that id's reranked logit, -inf if none). Device arrays.
+ * The _host variants take host arrays and run on the calling thread (no GPU needed).
+ */
+int dh_argmax_shard_keys(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
+                         int64_t id_offset, int64_t* keys, dh_stream_t s);
+int dh_argmax_merge(const int64_t* keys, int P, int64_t M, int32_t* argmax_id, float* logit,
+                    dh_stream_t s);
+int dh_argmax_shard_keys_host(const int32_t* rr_id, const float* rr_logit, int64_t M, int rerank,
+                              int64_t id_offset, int64_t* keys);
+int dh_argmax_merge_host(const int64_t* keys, int P, int64_t M, int32_t* argmax_id,
+                         float* logit);
+
+/*
  * The whole call from and to host memory (_apply_head_int2 end to end): copies x_host (bf16
  * [M, K]) into x_dev, runs dh_draft_head_argmax, copies
  * argmax [M], rr_id [M, rerank] and rr_logit [M, rerank] back into argmax_host, rr_id_host and
