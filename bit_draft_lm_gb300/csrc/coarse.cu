@@ -13,13 +13,14 @@ cudaError_t launch_coarse_i4g128(const CoarseArgs& a, int nsw, int grid, cudaStr
 cudaError_t launch_coarse_i4g64(const CoarseArgs& a, int nsw, int grid, cudaStream_t s);
 
 // Shared-memory plan for one launch; returns the weight ring depth (0 if nothing fits).
+// mt_cap: most hidden rows per pass (8, or fewer when the partial buffers of 8 do not fit).
 template <int BITS>
-static int plan_coarse(CoarseArgs& a, int max_smem, int nsw_max) {
+static int plan_coarse(CoarseArgs& a, int max_smem, int nsw_max, int mt_cap) {
   constexpr int SB = BITS == 2 ? 64 : 128;
   a.RB = a.K * BITS / 8;
   a.KG = a.K / a.G;
   a.NW = a.K / 256;
-  const int mt_max = a.M < 8 ? a.M : 8;
+  const int mt_max = a.M < mt_cap ? a.M : mt_cap;
   a.red_pitch = mt_max | 1;  // odd: a warp reading one column over 32 rows hits 32 banks
   const int red_buf = (a.NW + 1) * kBlockRows * a.red_pitch * 4;  // NW warps + zero-point slot
   const int wstage = kTileRows * SB;
@@ -60,6 +61,12 @@ cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, 
   // many hidden rows of an int2 head: one tensor-core pass instead of several warp-MMA passes
   if (cc.scratch != nullptr && coarse_wide_supports(cc))
     return launch_coarse_wide(cc, cc.scratch, num_sms, max_smem, s);
+  // int2 heads: the warp-specialised streaming kernel (tensor-map tiles); the warp-MMA kernel
+  // below takes the int4 head and any shape the streaming kernel's plan does not fit
+  if (coarse_stream_supports(cc)) {
+    const cudaError_t e = launch_coarse_stream(cc, num_sms, max_smem, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   CoarseArgs a{};
   a.x = static_cast<const uint16_t*>(cc.x);
   a.M = static_cast<int>(cc.M);
@@ -76,14 +83,21 @@ cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, 
   a.y = static_cast<uint16_t*>(cc.y);
   a.status = cc.status;
   if (cc.G != 64 && cc.G != 128) return cudaErrorInvalidValue;
-  const int nsw = cc.bits == 2 ? plan_coarse<2>(a, max_smem, 8) : plan_coarse<4>(a, max_smem, 4);
+  // passes of 8 hidden rows (one MMA column tile); where their partial buffers do not fit next
+  // to the rings (the int4 head with 64-wide groups at K = 5120), passes of 4, 2 or 1
+  int nsw = 0, pass_rows = 8;
+  for (; pass_rows >= 1; pass_rows /= 2) {
+    nsw = cc.bits == 2 ? plan_coarse<2>(a, max_smem, 8, pass_rows)
+                       : plan_coarse<4>(a, max_smem, 4, pass_rows);
+    if (nsw >= 2) break;
+  }
   if (nsw < 2) return cudaErrorInvalidValue;
   if (a.NW < 1 || a.NW > kCoarseMaxWarps || a.KG % 8) return cudaErrorInvalidValue;
   a.u16_mul = 1u << 16;
   const int grid = a.nblk < num_sms ? a.nblk : num_sms;
-  for (int m0 = 0; m0 < a.M; m0 += 8) {
+  for (int m0 = 0; m0 < a.M; m0 += pass_rows) {
     a.m0 = m0;
-    a.mt = a.M - m0 < 8 ? a.M - m0 : 8;
+    a.mt = a.M - m0 < pass_rows ? a.M - m0 : pass_rows;
     cudaError_t e;
     if (cc.bits == 2)
       e = cc.G == 128 ? launch_coarse_i2g128(a, nsw, grid, s) : launch_coarse_i2g64(a, nsw, grid, s);

@@ -67,6 +67,29 @@ def check_block_candidates(c, o_val, o_id, g_val, g_id, kcand):
     return mism
 
 
+def ambiguous_slots(c, kcand):
+    """How many (row, block, slot) selections the coarse tolerance leaves open: slot s of a block
+    (s < kcand, the oracle's values sorted descending) can hold another id only if its value is
+    within the tolerance of its neighbour above or below. An upper bound on the near-tie swaps,
+    whatever the data (a row whose values are all near-ties at its own scale has many)."""
+    M, N = c.shape
+    tol = coarse_tol(c)
+    n = 0
+    for m in range(M):
+        for b0 in range(0, N, 64):
+            v = c[m, b0:b0 + 64]
+            t = tol[m, b0:b0 + 64]
+            o = np.argsort(-v, kind="stable")
+            vs, ts = v[o], t[o]
+            gap = vs[:-1] - vs[1:]
+            close = gap <= np.maximum(ts[:-1], ts[1:])  # pair (s, s + 1) is a near-tie
+            k = min(kcand, v.size)
+            for s in range(k):
+                if (s > 0 and close[s - 1]) or (s < close.size and close[s]):
+                    n += 1
+    return n
+
+
 def rerank_tol(x_u16, W_u16, ids, e):
     x = bf16_to_f64(x_u16)
     tol = np.empty_like(e)

@@ -15,8 +15,8 @@ from bit_draft_lm_gb300 import build as dh_build
 from bit_draft_lm_gb300 import drafthead as dh
 from bit_draft_lm_gb300 import synth
 
-from _parity import (bf16_to_f64, check_block_candidates, coarse_tol, dev_bf16, host_u16,
-                     near_tie_rows, rerank_tol)
+from _parity import (ambiguous_slots, bf16_to_f64, check_block_candidates, coarse_tol, dev_bf16,
+                     host_u16, near_tie_rows, rerank_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -124,8 +124,9 @@ def test_coarse_topk_parity(M, K, N, G, bits, kcand, seed):
     mism = check_block_candidates(c, ov, oi, cv.cpu().numpy(), ci.cpu().numpy(), kcand)
     print(f"near-tie swaps M={M} K={K} N={N} G={G} bits={bits} kcand={kcand}: {mism} of "
           f"{ov.size} slots")
-    # every swap was checked to be a near-tie; they must stay rare
-    assert mism <= max(2, ov.size // 200), f"{mism} near-tie swaps"
+    # every swap was checked to be a near-tie; they must stay rare: fp32 accumulation order is
+    # their only source, measured at 0-3 swaps per case (9 in the 1.1 M slots of 72 rows)
+    assert mism <= max(2, ov.size // 1000), f"{mism} near-tie swaps"
     # coarse logits: bf16(c) within the coarse tolerance plus half a bf16 step
     yv = bf16_to_f64(host_u16(y))
     assert np.all(np.abs(yv - c) <= coarse_tol(c) + np.abs(c) * 2.0 ** -8)
@@ -506,7 +507,11 @@ def test_wide_dynamic_range_hidden_rows(M, bits, G):
     w_, dev, c, ov, oi = _run_case(M, K, N, G, bits, kcand, 0, w=w)
     W, packed, S, ZS, x, y, ws, cv, ci = dev
     mism = check_block_candidates(c, ov, oi, cv.cpu().numpy(), ci.cpu().numpy(), kcand)
-    assert mism <= 2
+    # where the spikes cancel, a row's coarse values are all near-ties at the row's own scale
+    # (the tolerance's RMS floor), so swaps are bounded by the oracle's open selections
+    amb = ambiguous_slots(c, kcand)
+    print(f"wide-range rows M={M}: {mism} near-tie swaps, {amb} open selections")
+    assert mism <= max(2, amb)
     yv = bf16_to_f64(host_u16(y))
     assert np.all(np.abs(yv - c) <= coarse_tol(c) + np.abs(c) * 2.0 ** -8)
     rr, rl, am = dh.dh_draft_head_rerank_argmax(x, W, cv, ci, R, workspace=ws)
