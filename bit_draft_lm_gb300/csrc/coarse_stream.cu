@@ -3,8 +3,8 @@
 // for sm_103a. A warp-specialised streaming kernel:
 //
 //  * Persistent grid, one CTA per SM, walking 64-row candidate blocks b = blockIdx.x + j * grid;
-//    each block is four 16-row tiles. NW = K / 256 MMA warps, one producer warp and nb epilogue
-//    warps (nb = the partial buffers, 1 or 2).
+//    each block is four 16-row tiles. NW = K / 256 MMA warps, one producer warp and three
+//    epilogue warps.
 //  * The producer streams the packed head with ONE tensor-map copy per 16-row tile (TMA): a 3-D
 //    view of the packed rows -- dim 0 the 64 bytes of a warp's strip, dim 1 the rows (stride
 //    K/4), dim 2 the NW strips (stride 64) -- and a {64, 16, NW} box land the whole tile in the
@@ -28,11 +28,13 @@
 //    S * (XS + sum x v / 4) - ZS * XS = S * sum x v / 4 + (S - ZS) * XS, so the MMA warps
 //    accumulate S * sum x v (the scale on the accumulator, never on the weight tile) and the
 //    zero-point part sum_g (S - ZS) XS is a short bf16 MMA chain per tile, run by the epilogue.
-//  * Epilogue warp e owns partial buffer e, so it takes blocks e, e + nb, ... in order: it waits
-//    for the block's NW partial sets, adds the zero-point part, sums the partials of each row in
-//    a fixed order (deterministic), selects the block's top-KCAND per hidden row with warp
-//    reductions (max key, lowest row on ties), writes the candidates and releases the buffer and
-//    the S/ZS stage.
+//  * The three epilogue warps take every block in order: they wait for its NW partial sets,
+//    compute the zero-point part (split by tile, handed over through an mbarrier), then split the
+//    hidden rows: each sums the partials of its rows in a fixed order (deterministic), selects the
+//    block's top-KCAND with warp reductions (max key, lowest row on ties) and writes the
+//    candidates; the last of the three releases the partial buffer and the S/ZS stage.
+//  * Waits test once, then poll with __nanosleep between tests: a waiting warp takes no issue
+//    slots from the MMA warps of its SM sub-partition.
 // Every wait is bounded (kWaitLimitNs): a wait that runs out marks the launch failed in the status
 // word and every later wait returns at once; the producer then waits (bounded) for its copies in
 // flight before the CTA exits.
@@ -54,8 +56,9 @@ namespace dh {
 namespace {
 
 constexpr int kSMaxNW = 20;      // K <= 5120
-constexpr int kSMaxEpi = 2;      // epilogue warps = partial buffers
-constexpr int kSMaxThreads = (kSMaxNW + 1 + kSMaxEpi) * 32;
+constexpr int kEpi = 3;          // epilogue warps
+constexpr int kSMaxRed = 2;      // partial buffers
+constexpr int kSMaxThreads = (kSMaxNW + 1 + kEpi) * 32;
 constexpr int kSMaxStages = 8;   // packed tile stages
 constexpr int kSMaxSZ = 4;       // S/ZS block stages
 constexpr int kStrip = 64;       // packed bytes of a warp's strip of one row
@@ -78,7 +81,7 @@ struct StreamArgs {
   uint16_t* y;  // bf16 [M, N] or nullptr
   uint32_t* status;
   uint32_t u16_mul;  // 2^16: bf16 bits -> fp32 as an integer multiply (FMA pipe, not ALU)
-  int ns, nsb, nb, rp;  // tile stages, S/ZS stages, partial buffers (= epilogue warps), row pitch
+  int ns, nsb, nb, rp;  // tile stages, S/ZS stages, partial buffers, partial row pitch
   int off_bars, off_xs, off_zb, off_sz, off_red, off_zp, off_ring;
 };
 
@@ -100,9 +103,10 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
   uint64_t* tile_empty = tile_full + kSMaxStages;                      // [kSMaxStages]
   uint64_t* sz_full = tile_empty + kSMaxStages;                        // [kSMaxSZ]
   uint64_t* sz_empty = sz_full + kSMaxSZ;                              // [kSMaxSZ]
-  uint64_t* red_full = sz_empty + kSMaxSZ;                             // [kSMaxEpi]
-  uint64_t* red_empty = red_full + kSMaxEpi;                           // [kSMaxEpi]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + kSMaxEpi);
+  uint64_t* red_full = sz_empty + kSMaxSZ;                             // [kSMaxRed]
+  uint64_t* red_empty = red_full + kSMaxRed;                           // [kSMaxRed]
+  uint64_t* zp_done = red_empty + kSMaxRed;                            // [kSMaxRed]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(zp_done + kSMaxRed);
   float* xs_part = reinterpret_cast<float*>(sm + a.off_xs);  // [NW][8][NQ] strip group sums
   float* xs_full = xs_part + NW * 8 * NQ;                    // [mt][KG] group sums XS
   uint2* zb = reinterpret_cast<uint2*>(sm + a.off_zb);  // [KG/8][3][mt][4] zero-point B frags
@@ -120,14 +124,16 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     return (static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x)) * kBlockRows;
   };
 
-  // Bounded wait of one thread; false once the launch is aborted (its own timeout or another
-  // thread's).
-  auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (mbar_try_wait(bar, parity)) return true;
+  // Bounded wait of one thread: one test, then polls spaced by `sleep_ns` of __nanosleep (a
+  // sleeping warp takes no issue slots from the MMA warps of its SM sub-partition). False once the
+  // launch is aborted (its own timeout or another thread's).
+  auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t sleep_ns) -> bool {
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
+      __nanosleep(sleep_ns);
+      if (mbar_test_wait(bar, parity)) return true;
       if (*abort_flag) return false;
-      if (mbar_try_wait(bar, parity)) return true;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
         set_status(a.status, DH_DEV_WAIT_TIMEOUT);
@@ -138,9 +144,9 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
   // The same for a whole warp: lane 0 waits, the outcome is broadcast (every lane takes the same
   // path: the loops hold warp-wide MMAs and reductions), then every lane observes the completed
   // phase itself (acquire).
-  auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity, uint32_t sleep_ns) -> bool {
     int ok = 1;
-    if (lane == 0) ok = wait1(bar, parity) ? 1 : 0;
+    if (lane == 0) ok = wait1(bar, parity, sleep_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) mbar_test_wait(bar, parity);
     return ok != 0;
@@ -152,14 +158,13 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
       mbar_init(&tile_full[q], 1u);
       mbar_init(&tile_empty[q], static_cast<uint32_t>(NW));
     }
-    for (int q = 0; q < kSMaxSZ; ++q) {
-      mbar_init(&sz_full[q], 1u);
-      mbar_init(&sz_empty[q], 1u);
-    }
-    for (int q = 0; q < kSMaxEpi; ++q) {
+    for (int q = 0; q < kSMaxSZ; ++q) mbar_init(&sz_full[q], 1u);
+    for (int q = 0; q < kSMaxRed; ++q) {
       mbar_init(&red_full[q], static_cast<uint32_t>(NW));
-      mbar_init(&red_empty[q], 1u);
+      mbar_init(&red_empty[q], static_cast<uint32_t>(kEpi));
+      mbar_init(&zp_done[q], static_cast<uint32_t>(kEpi));
     }
+    for (int q = 0; q < kSMaxSZ; ++q) mbar_init(&sz_empty[q], static_cast<uint32_t>(kEpi));
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -301,7 +306,7 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
       int s = 0, sph = 0, st = 0, stph = 0;  // ring positions and their phase parities
       for (int lb = 0; lb < my_blocks; ++lb) {
         const int row0 = block_row0(lb);
-        if (lb >= nsb && !wait1(&sz_empty[st], static_cast<uint32_t>(stph ^ 1))) break;
+        if (lb >= nsb && !wait1(&sz_empty[st], static_cast<uint32_t>(stph ^ 1), 256u)) break;
         {
           const int rows = a.N - row0 > kBlockRows ? kBlockRows : a.N - row0;
           const uint32_t bytes = static_cast<uint32_t>(rows * KG * 2);  // KG % 8 == 0
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
         bool ok = true;
         for (int t = 0; t < kTilesPerBlock; ++t) {
           const int tau = 4 * lb + t;
-          if (tau >= ns && !wait1(&tile_empty[s], static_cast<uint32_t>(sph ^ 1))) {
+          if (tau >= ns && !wait1(&tile_empty[s], static_cast<uint32_t>(sph ^ 1), 128u)) {
             ok = false;
             break;
           }
@@ -347,18 +352,19 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     }
     __syncwarp();
   } else if (warp > prod_warp) {
-    // ---- epilogue warp e: blocks e, e + nb, ... (partial buffer e) ---------------------------
+    // ---- epilogue warps e = 0 .. kEpi - 1: every block, in order; warp e computes the zero point
+    // of tiles e, e + kEpi, ... and then selects for hidden rows e, e + kEpi, ...
     const int e = warp - prod_warp - 1;
-    float* zp = zpb + e * kBlockRows * rp;
-    const float* rbuf = red + e * NW * red_wstride;
-    int ph = 0;
-    for (int lb = e; lb < my_blocks; lb += nb, ph ^= 1) {
-      if (!wait_warp(&red_full[e], static_cast<uint32_t>(ph))) break;
+    int buf = 0, ph = 0;
+    for (int lb = 0; lb < my_blocks; ++lb) {
+      if (!wait_warp(&red_full[buf], static_cast<uint32_t>(ph), 256u)) break;
       const int st = lb % nsb;
       const unsigned char* stage = sz + st * 2 * sz_half;
       // the stage's copies landed before the MMA warps' arrivals; observe their phase here too
-      // (it cannot move on before this warp releases the stage)
+      // (it cannot move on before the epilogue releases the stage)
       mbar_test_wait(&sz_full[st], static_cast<uint32_t>(lb / nsb) & 1u);
+      float* zp = zpb + buf * kBlockRows * rp;
+      const float* rbuf = red + buf * NW * red_wstride;
       // zero-point part of the block, per 16-row tile: A = [S | ZS] rows (bf16, as stored),
       // B = [XS ; -XS] in three bf16 parts; D rows g, g + 8 x hidden rows 2c, 2c + 1
       {
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
         const bool zlive = g < mt;
         const int row8 = 8 * KG * 2;
 #pragma unroll 1
-        for (int t = 0; t < kTilesPerBlock; ++t) {
+        for (int t = e; t < kTilesPerBlock; t += kEpi) {
           float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
           const unsigned char* srow = stage + (t * kTileRows + g) * KG * 2 + 4 * c;
           for (int kk = 0; kk < KG / 8; ++kk) {
@@ -395,10 +401,16 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
           }
         }
       }
+      // every epilogue warp's tiles of the zero point are written
       __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        mbar_arrive(&zp_done[buf]);
+      }
+      if (!wait_warp(&zp_done[buf], static_cast<uint32_t>(ph), 64u)) break;
       const int b = static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x);
       const int n0 = b * kBlockRows + lane;
-      for (int m = 0; m < mt; ++m) {
+      for (int m = e; m < mt; m += kEpi) {
         float v[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -456,9 +468,10 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&red_empty[e]);  // the partial buffer and the zero-point scratch
-        mbar_arrive(&sz_empty[st]);  // the S/ZS stage (the MMA warps were done with it)
+        mbar_arrive(&red_empty[buf]);  // the partial buffer and the zero-point scratch
+        mbar_arrive(&sz_empty[st]);    // the S/ZS stage (the MMA warps were done with it)
       }
+      if (++buf == nb) { buf = 0; ph ^= 1; }
     }
   } else {
     // ---- MMA warps ---------------------------------------------------------------------------
@@ -481,14 +494,14 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     const int soa = so_g + 2 * s_col(qa), sob = so_g + 2 * s_col(qa + 1 < NQ ? qa + 1 : qa);
     int s = 0, sph = 0, st = 0, stph = 0, buf = 0, rph = 0;
     for (int lb = 0; lb < my_blocks; ++lb) {
-      bool ok = wait_warp(&sz_full[st], static_cast<uint32_t>(stph));
-      if (ok && lb >= nb) ok = wait_warp(&red_empty[buf], static_cast<uint32_t>(rph ^ 1));
+      bool ok = wait_warp(&sz_full[st], static_cast<uint32_t>(stph), 64u);
+      if (ok && lb >= nb) ok = wait_warp(&red_empty[buf], static_cast<uint32_t>(rph ^ 1), 64u);
       if (!ok) break;
       const unsigned char* stage = sz + st * 2 * sz_half;
       float* rwb = red + buf * NW * red_wstride + warp * red_wstride + g * rp + (MT1 ? 0 : 2 * c);
-#pragma unroll 1
+#pragma unroll
       for (int t = 0; t < kTilesPerBlock; ++t) {
-        if (!wait_warp(&tile_full[s], static_cast<uint32_t>(sph))) {
+        if (!wait_warp(&tile_full[s], static_cast<uint32_t>(sph), 32u)) {
           ok = false;
           break;
         }
@@ -628,7 +641,7 @@ bool plan_stream(StreamArgs& a, int mt, int max_smem, int* smem) {
     const int nb = pl[0], nsb = pl[1], ns = pl[2];
     int off = 0;
     a.off_bars = off;
-    off += (2 * kSMaxStages + 2 * kSMaxSZ + 2 * kSMaxEpi) * 8 + 16;
+    off += (2 * kSMaxStages + 2 * kSMaxSZ + 3 * kSMaxRed) * 8 + 16;
     a.off_xs = off = round16(off);
     off += NW * 8 * 4 * 4 + mt * a.KG * 4;
     a.off_zb = off = round16(off);
@@ -662,7 +675,7 @@ cudaError_t launch_stream_kernel(const CUtensorMap& map, const StreamArgs& a, in
   // in the stream finishes; everything else waits for it (griddepcontrol.wait)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((a.NW + 1 + a.nb) * 32);
+  cfg.blockDim = dim3((a.NW + 1 + kEpi) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
