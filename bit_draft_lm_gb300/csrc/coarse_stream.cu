@@ -3,19 +3,20 @@
 // for sm_103a. A warp-specialised streaming kernel:
 //
 //  * Persistent grid, one CTA per SM, walking 64-row candidate blocks b = blockIdx.x + j * grid;
-//    each block is four 16-row tiles. NW = K / 256 MMA warps, one producer warp and three
-//    epilogue warps.
-//  * The producer streams the packed head with ONE tensor-map copy per 16-row tile (TMA): a 3-D
-//    view of the packed rows -- dim 0 the 64 bytes of a warp's strip, dim 1 the rows (stride
-//    K/4), dim 2 the NW strips (stride 64) -- and a {64, 16, NW} box land the whole tile in the
-//    layout each MMA warp reads, [warp][16 rows][64 bytes], into a ring of ns stages (a full/empty
-//    mbarrier pair per stage); rows past N come in as zeros. It also brings each block's S and ZS
-//    rows (two bulk copies) into a ring of nsb block stages.
+//    each block is four 16-row tiles. NW = K / 256 MMA warps and three epilogue warps.
+//  * The packed head streams in with ONE tensor-map copy per 16-row tile (TMA): a 3-D view of the
+//    packed rows -- dim 0 the 64 bytes of a warp's strip, dim 1 the rows (stride K/4), dim 2 the
+//    NW strips (stride 64) -- and a {64, 16, NW} box land the whole tile in the layout each MMA
+//    warp reads, [warp][16 rows][64 bytes], into a ring of ns stages; rows past N come in as
+//    zeros. There is no producer warp: the last MMA warp to release a stage (an arrival counter)
+//    issues that stage's next copy, so no warp waits to refill the ring. Each block's S and ZS rows
+//    (two bulk copies) come into a ring of nsb block stages the same way, refilled by the last
+//    epilogue warp done with a block.
 //  * MMA warp w owns the same 256 k-values of every vocab row (bytes [64w, 64w + 64) of each
-//    packed row): its x fragments stay in registers for the whole launch. Per tile it waits for
-//    the stage, reads its strip (two 16-byte loads per lane, conflict-free), dequantises and
+//    packed row): its x fragments stay in registers for the whole launch. Per tile it checks the
+//    stage, reads its strip (two 16-byte loads per lane, conflict-free), dequantises and
 //    multiplies (below), folds the per-group scale into its accumulator, writes its partial sums
-//    of the tile's rows and releases the stage. Nothing else: no copies, no epilogue.
+//    of the tile's rows and releases the stage. Nothing else: no copies to wait for, no epilogue.
 //  * Dequant in place, as f16 subnormals: in an f16 pair every bit of the low byte of each half
 //    is mantissa, so for a packed 32-bit word t the AND of t with plane p's code mask is the f16
 //    pair (byte 0's code, byte 2's code) * 2^(2p - 24) exactly, and the same AND of t >> 8 gives
@@ -32,11 +33,10 @@
 //    compute the zero-point part (split by tile, handed over through an mbarrier), then split the
 //    hidden rows: each sums the partials of its rows in a fixed order (deterministic), selects the
 //    block's top-KCAND with warp reductions (max key, lowest row on ties) and writes the
-//    candidates; the last of the three releases the partial buffer and the S/ZS stage.
-//  * Waits test once, then poll with __nanosleep between tests: a waiting warp takes no issue
-//    slots from the MMA warps of its SM sub-partition.
+//    candidates. They poll with __nanosleep between tests, so that they take almost no issue slots
+//    from the MMA warps; two partial buffers hide their wake-up latency.
 // Every wait is bounded (kWaitLimitNs): a wait that runs out marks the launch failed in the status
-// word and every later wait returns at once; the producer then waits (bounded) for its copies in
+// word and every later wait returns at once; thread 0 then waits (bounded) for the copies still in
 // flight before the CTA exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -58,7 +58,7 @@ namespace {
 constexpr int kSMaxNW = 20;      // K <= 5120
 constexpr int kEpi = 3;          // epilogue warps
 constexpr int kSMaxRed = 2;      // partial buffers
-constexpr int kSMaxThreads = (kSMaxNW + 1 + kEpi) * 32;
+constexpr int kSMaxThreads = (kSMaxNW + kEpi) * 32;
 constexpr int kSMaxStages = 8;   // packed tile stages
 constexpr int kSMaxSZ = 4;       // S/ZS block stages
 constexpr int kStrip = 64;       // packed bytes of a warp's strip of one row
@@ -100,13 +100,15 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
   const int ns = a.ns, nsb = a.nsb, nb = a.nb;
 
   uint64_t* tile_full = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kSMaxStages]
-  uint64_t* tile_empty = tile_full + kSMaxStages;                      // [kSMaxStages]
-  uint64_t* sz_full = tile_empty + kSMaxStages;                        // [kSMaxSZ]
-  uint64_t* sz_empty = sz_full + kSMaxSZ;                              // [kSMaxSZ]
-  uint64_t* red_full = sz_empty + kSMaxSZ;                             // [kSMaxRed]
+  uint64_t* sz_full = tile_full + kSMaxStages;                         // [kSMaxSZ]
+  uint64_t* red_full = sz_full + kSMaxSZ;                              // [kSMaxRed]
   uint64_t* red_empty = red_full + kSMaxRed;                           // [kSMaxRed]
   uint64_t* zp_done = red_empty + kSMaxRed;                            // [kSMaxRed]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(zp_done + kSMaxRed);
+  int* tcnt = reinterpret_cast<int*>(zp_done + kSMaxRed);  // [kSMaxStages] releases of a stage
+  int* tiss = tcnt + kSMaxStages;                          // [kSMaxStages] last tile issued
+  int* scnt = tiss + kSMaxStages;                          // [kSMaxSZ] epilogue warps done
+  int* siss = scnt + kSMaxSZ;                              // [kSMaxSZ] last block issued
+  volatile int* abort_flag = siss + kSMaxSZ;
   float* xs_part = reinterpret_cast<float*>(sm + a.off_xs);  // [NW][8][NQ] strip group sums
   float* xs_full = xs_part + NW * 8 * NQ;                    // [mt][KG] group sums XS
   uint2* zb = reinterpret_cast<uint2*>(sm + a.off_zb);  // [KG/8][3][mt][4] zero-point B frags
@@ -120,60 +122,90 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
 
   const int my_blocks = (a.nblk - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                         static_cast<int>(gridDim.x);
+  const int ntiles = kTilesPerBlock * my_blocks;
   auto block_row0 = [&](int lb) {
     return (static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x)) * kBlockRows;
   };
 
-  // Bounded wait of one thread: one test, then polls spaced by `sleep_ns` of __nanosleep (a
-  // sleeping warp takes no issue slots from the MMA warps of its SM sub-partition). False once the
-  // launch is aborted (its own timeout or another thread's).
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(a.status, DH_DEV_WAIT_TIMEOUT);
+  };
+  // Bounded wait of one thread: tests spaced by `sleep_ns` of __nanosleep (0: a plain spin),
+  // the abort flag and the clock looked at every 64 tests. False once the launch is aborted (its
+  // own timeout or another thread's).
   auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t sleep_ns) -> bool {
-    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (true) {
-      __nanosleep(sleep_ns);
+    for (uint32_t it = 1;; ++it) {
       if (mbar_test_wait(bar, parity)) return true;
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        set_status(a.status, DH_DEV_WAIT_TIMEOUT);
-        return false;
+      if (sleep_ns) __nanosleep(sleep_ns);
+      if ((it & 63u) == 0u) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          fail();
+          return false;
+        }
       }
     }
   };
-  // The same for a whole warp: lane 0 waits, the outcome is broadcast (every lane takes the same
-  // path: the loops hold warp-wide MMAs and reductions), then every lane observes the completed
-  // phase itself (acquire).
+  // The same for a whole warp (every lane takes the same path: the loops hold warp-wide MMAs and
+  // reductions). Fast path: every lane tests the phase itself and one vote says all saw it
+  // complete; else lane 0 waits, the outcome is broadcast and every lane observes the phase.
   auto wait_warp = [&](uint64_t* bar, uint32_t parity, uint32_t sleep_ns) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     int ok = 1;
     if (lane == 0) ok = wait1(bar, parity, sleep_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) mbar_test_wait(bar, parity);
     return ok != 0;
   };
+  // Tile tau of this CTA into ring stage s (one thread). A tile wholly past N (the head's last
+  // block) is not copied: its phase completes at once and the MMA warps read stale codes for rows
+  // the epilogue ignores.
+  auto issue_tile = [&](int tau, int s) {
+    tiss[s] = tau;
+    const int row = block_row0(tau / kTilesPerBlock) + kTileRows * (tau % kTilesPerBlock);
+    if (row < a.N) {
+      mbar_arrive_expect_tx(&tile_full[s], static_cast<uint32_t>(tstage));
+      tma_load_3d(ring + s * tstage, &tmap, 0, row, 0, &tile_full[s]);
+    } else {
+      mbar_arrive(&tile_full[s]);
+    }
+  };
+  // S and ZS rows of local block lb into block stage st (one thread).
+  auto issue_sz = [&](int lb, int st) {
+    siss[st] = lb;
+    const int row0 = block_row0(lb);
+    const int rows = a.N - row0 > kBlockRows ? kBlockRows : a.N - row0;
+    const uint32_t bytes = static_cast<uint32_t>(rows * KG * 2);  // KG % 8 == 0
+    unsigned char* dst = sz + st * 2 * sz_half;
+    mbar_arrive_expect_tx(&sz_full[st], 2u * bytes);
+    bulk_g2s(dst, a.S + static_cast<int64_t>(row0) * KG, bytes, &sz_full[st]);
+    bulk_g2s(dst + sz_half, a.ZS + static_cast<int64_t>(row0) * KG, bytes, &sz_full[st]);
+  };
 
-  const int prod_warp = NW;  // then the epilogue warps NW + 1 .. NW + nb
   if (threadIdx.x == 0) {
     for (int q = 0; q < kSMaxStages; ++q) {
       mbar_init(&tile_full[q], 1u);
-      mbar_init(&tile_empty[q], static_cast<uint32_t>(NW));
+      tcnt[q] = 0;
+      tiss[q] = -1;
     }
-    for (int q = 0; q < kSMaxSZ; ++q) mbar_init(&sz_full[q], 1u);
+    for (int q = 0; q < kSMaxSZ; ++q) {
+      mbar_init(&sz_full[q], 1u);
+      scnt[q] = 0;
+      siss[q] = -1;
+    }
     for (int q = 0; q < kSMaxRed; ++q) {
       mbar_init(&red_full[q], static_cast<uint32_t>(NW));
       mbar_init(&red_empty[q], static_cast<uint32_t>(kEpi));
       mbar_init(&zp_done[q], static_cast<uint32_t>(kEpi));
     }
-    for (int q = 0; q < kSMaxSZ; ++q) mbar_init(&sz_empty[q], static_cast<uint32_t>(kEpi));
     *abort_flag = 0;
     mbar_fence_init();
-  }
-  // Before griddepcontrol.wait only L2 is warmed (the preceding kernel may have written the
-  // weights; L2 is coherent): the first tiles and S/ZS stages.
-  if (warp == prod_warp && lane == 0) {
+    // Before griddepcontrol.wait only L2 is warmed (the preceding kernel may have written the
+    // weights; L2 is coherent): the first tiles and S/ZS stages.
     tma_prefetch_map(&tmap);
-    const int ntl = 4 * my_blocks;
-    for (int tau = 0; tau < ns && tau < ntl; ++tau)
+    for (int tau = 0; tau < ns && tau < ntiles; ++tau)
       tma_prefetch_l2_3d(&tmap, 0, block_row0(tau >> 2) + kTileRows * (tau & 3), 0);
     for (int lb = 0; lb < nsb && lb < my_blocks; ++lb) {
       const int row0 = block_row0(lb);
@@ -183,6 +215,10 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     }
   }
   grid_dependency_wait();
+  if (threadIdx.x == 0) {
+    for (int lb = 0; lb < nsb && lb < my_blocks; ++lb) issue_sz(lb, lb);
+    for (int tau = 0; tau < ns && tau < ntiles; ++tau) issue_tile(tau, tau);
+  }
 
   // ---- MMA warps: x fragments of the strip (B operand), strip sums of each scale group --------
   const int strip_byte = warp * kStrip;
@@ -299,65 +335,13 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
   }
   __syncthreads();
 
-  if (warp == prod_warp) {
-    // ---- producer: S/ZS of each block, then its four tiles, in the order they are consumed ----
-    int issued = 0, issued_sz = 0;
-    if (lane == 0) {
-      int s = 0, sph = 0, st = 0, stph = 0;  // ring positions and their phase parities
-      for (int lb = 0; lb < my_blocks; ++lb) {
-        const int row0 = block_row0(lb);
-        if (lb >= nsb && !wait1(&sz_empty[st], static_cast<uint32_t>(stph ^ 1), 256u)) break;
-        {
-          const int rows = a.N - row0 > kBlockRows ? kBlockRows : a.N - row0;
-          const uint32_t bytes = static_cast<uint32_t>(rows * KG * 2);  // KG % 8 == 0
-          unsigned char* dst = sz + st * 2 * sz_half;
-          mbar_arrive_expect_tx(&sz_full[st], 2u * bytes);
-          bulk_g2s(dst, a.S + static_cast<int64_t>(row0) * KG, bytes, &sz_full[st]);
-          bulk_g2s(dst + sz_half, a.ZS + static_cast<int64_t>(row0) * KG, bytes, &sz_full[st]);
-          issued_sz = lb + 1;
-        }
-        if (++st == nsb) { st = 0; stph ^= 1; }
-        bool ok = true;
-        for (int t = 0; t < kTilesPerBlock; ++t) {
-          const int tau = 4 * lb + t;
-          if (tau >= ns && !wait1(&tile_empty[s], static_cast<uint32_t>(sph ^ 1), 128u)) {
-            ok = false;
-            break;
-          }
-          if (row0 + kTileRows * t < a.N) {  // rows past N arrive as zeros
-            mbar_arrive_expect_tx(&tile_full[s], static_cast<uint32_t>(tstage));
-            tma_load_3d(ring + s * tstage, &tmap, 0, row0 + kTileRows * t, 0, &tile_full[s]);
-          } else {
-            // a tile wholly past N (the head's last block): nothing to copy; the MMA warps read
-            // stale codes for rows the epilogue ignores
-            mbar_arrive(&tile_full[s]);
-          }
-          issued = tau + 1;
-          if (++s == ns) { s = 0; sph ^= 1; }
-        }
-        if (!ok) break;
-      }
-      // After an abort, copies may still be in flight: they land before the CTA's shared memory
-      // goes away (bounded waits on the last phase each stage was given).
-      if (*abort_flag) {
-        for (int q = 0; q < ns && q < issued; ++q) {
-          const int last = issued - 1 - ((issued - 1 - q) % ns);
-          mbar_wait_bounded(&tile_full[q], static_cast<uint32_t>(last / ns) & 1u);
-        }
-        for (int q = 0; q < nsb && q < issued_sz; ++q) {
-          const int last = issued_sz - 1 - ((issued_sz - 1 - q) % nsb);
-          mbar_wait_bounded(&sz_full[q], static_cast<uint32_t>(last / nsb) & 1u);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp > prod_warp) {
+  if (warp >= NW) {
     // ---- epilogue warps e = 0 .. kEpi - 1: every block, in order; warp e computes the zero point
     // of tiles e, e + kEpi, ... and then selects for hidden rows e, e + kEpi, ...
-    const int e = warp - prod_warp - 1;
+    const int e = warp - NW;
     int buf = 0, ph = 0;
     for (int lb = 0; lb < my_blocks; ++lb) {
-      if (!wait_warp(&red_full[buf], static_cast<uint32_t>(ph), 256u)) break;
+      if (!wait_warp(&red_full[buf], static_cast<uint32_t>(ph), 1000u)) break;
       const int st = lb % nsb;
       const unsigned char* stage = sz + st * 2 * sz_half;
       // the stage's copies landed before the MMA warps' arrivals; observe their phase here too
@@ -407,7 +391,7 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
         __threadfence_block();
         mbar_arrive(&zp_done[buf]);
       }
-      if (!wait_warp(&zp_done[buf], static_cast<uint32_t>(ph), 64u)) break;
+      if (!wait_warp(&zp_done[buf], static_cast<uint32_t>(ph), 100u)) break;
       const int b = static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x);
       const int n0 = b * kBlockRows + lane;
       for (int m = e; m < mt; m += kEpi) {
@@ -468,8 +452,18 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
       }
       __syncwarp();
       if (lane == 0) {
+        __threadfence_block();
         mbar_arrive(&red_empty[buf]);  // the partial buffer and the zero-point scratch
-        mbar_arrive(&sz_empty[st]);    // the S/ZS stage (the MMA warps were done with it)
+        // the S/ZS stage: the MMA warps were done with it before the block's partials were
+        // complete; the last epilogue warp done with the block refills it
+        if (atomicAdd(&scnt[st], 1) == kEpi - 1) {
+          scnt[st] = 0;
+          __threadfence_block();
+          if (lb + nsb < my_blocks) {
+            fence_proxy_async_smem();  // the stage's reads come before the copy's writes
+            issue_sz(lb + nsb, st);
+          }
+        }
       }
       if (++buf == nb) { buf = 0; ph ^= 1; }
     }
@@ -494,14 +488,14 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     const int soa = so_g + 2 * s_col(qa), sob = so_g + 2 * s_col(qa + 1 < NQ ? qa + 1 : qa);
     int s = 0, sph = 0, st = 0, stph = 0, buf = 0, rph = 0;
     for (int lb = 0; lb < my_blocks; ++lb) {
-      bool ok = wait_warp(&sz_full[st], static_cast<uint32_t>(stph), 64u);
-      if (ok && lb >= nb) ok = wait_warp(&red_empty[buf], static_cast<uint32_t>(rph ^ 1), 64u);
+      bool ok = wait_warp(&sz_full[st], static_cast<uint32_t>(stph), 0u);
+      if (ok && lb >= nb) ok = wait_warp(&red_empty[buf], static_cast<uint32_t>(rph ^ 1), 0u);
       if (!ok) break;
       const unsigned char* stage = sz + st * 2 * sz_half;
       float* rwb = red + buf * NW * red_wstride + warp * red_wstride + g * rp + (MT1 ? 0 : 2 * c);
 #pragma unroll
       for (int t = 0; t < kTilesPerBlock; ++t) {
-        if (!wait_warp(&tile_full[s], static_cast<uint32_t>(sph), 32u)) {
+        if (!wait_warp(&tile_full[s], static_cast<uint32_t>(sph), 0u)) {
           ok = false;
           break;
         }
@@ -571,9 +565,21 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
             acc[3] = fmaf(sg8, d[3], acc[3]);
           }
         }
-        // the stage has been read (every lane's loads were consumed above)
+        // the stage has been read (every lane's loads were consumed above); the last of the NW
+        // warps to release it issues its next tile
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tile_empty[s]);
+        if (lane == 0) {
+          __threadfence_block();
+          if (atomicAdd(&tcnt[s], 1) == NW - 1) {
+            tcnt[s] = 0;
+            __threadfence_block();
+            const int nxt = kTilesPerBlock * lb + t + ns;
+            if (nxt < ntiles) {
+              fence_proxy_async_smem();  // the stage's reads come before the copy's writes
+              issue_tile(nxt, s);
+            }
+          }
+        }
         if (++s == ns) { s = 0; sph ^= 1; }
         // partials in logit units, D layout: acc[0..1] = row g, hidden rows 2c, 2c+1;
         // acc[2..3] = row g + 8 (MT1: acc[0], acc[2] in lane c = 0)
@@ -606,6 +612,14 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     }
   }
   __syncthreads();
+  // After an abort, copies may still be in flight: they land before the CTA's shared memory goes
+  // away (bounded waits on the last phase each stage was given; completed phases return at once).
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int q = 0; q < ns; ++q)
+      if (tiss[q] >= 0) mbar_wait_bounded(&tile_full[q], static_cast<uint32_t>(tiss[q] / ns) & 1u);
+    for (int q = 0; q < nsb; ++q)
+      if (siss[q] >= 0) mbar_wait_bounded(&sz_full[q], static_cast<uint32_t>(siss[q] / nsb) & 1u);
+  }
 }
 
 // ---- host side ----------------------------------------------------------------------------------
@@ -641,7 +655,7 @@ bool plan_stream(StreamArgs& a, int mt, int max_smem, int* smem) {
     const int nb = pl[0], nsb = pl[1], ns = pl[2];
     int off = 0;
     a.off_bars = off;
-    off += (2 * kSMaxStages + 2 * kSMaxSZ + 3 * kSMaxRed) * 8 + 16;
+    off += (kSMaxStages + kSMaxSZ + 3 * kSMaxRed) * 8 + (2 * kSMaxStages + 2 * kSMaxSZ + 1) * 4;
     a.off_xs = off = round16(off);
     off += NW * 8 * 4 * 4 + mt * a.KG * 4;
     a.off_zb = off = round16(off);
@@ -675,7 +689,7 @@ cudaError_t launch_stream_kernel(const CUtensorMap& map, const StreamArgs& a, in
   // in the stream finishes; everything else waits for it (griddepcontrol.wait)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((a.NW + 1 + kEpi) * 32);
+  cfg.blockDim = dim3((a.NW + kEpi) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
