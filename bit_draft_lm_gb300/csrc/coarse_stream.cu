@@ -34,7 +34,7 @@
 //    hidden rows: each sums the partials of its rows in a fixed order (deterministic), selects the
 //    block's top-KCAND with warp reductions (max key, lowest row on ties) and writes the
 //    candidates. They poll with __nanosleep between tests, so that they take almost no issue slots
-//    from the MMA warps; two partial buffers hide their wake-up latency.
+//    from the MMA warps; up to four partial buffers hide their wake-up latency.
 // Every wait is bounded (kWaitLimitNs): a wait that runs out marks the launch failed in the status
 // word and every later wait returns at once; thread 0 then waits (bounded) for the copies still in
 // flight before the CTA exits.
@@ -57,7 +57,7 @@ namespace {
 
 constexpr int kSMaxNW = 20;      // K <= 5120
 constexpr int kEpi = 3;          // epilogue warps
-constexpr int kSMaxRed = 2;      // partial buffers
+constexpr int kSMaxRed = 4;      // partial buffers
 constexpr int kSMaxThreads = (kSMaxNW + kEpi) * 32;
 constexpr int kSMaxStages = 8;   // packed tile stages
 constexpr int kSMaxSZ = 4;       // S/ZS block stages
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     const int e = warp - NW;
     int buf = 0, ph = 0;
     for (int lb = 0; lb < my_blocks; ++lb) {
-      if (!wait_warp(&red_full[buf], static_cast<uint32_t>(ph), 1000u)) break;
+      if (!wait_warp(&red_full[buf], static_cast<uint32_t>(ph), 128u)) break;
       const int st = lb % nsb;
       const unsigned char* stage = sz + st * 2 * sz_half;
       // the stage's copies landed before the MMA warps' arrivals; observe their phase here too
@@ -357,7 +357,8 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
         const int row8 = 8 * KG * 2;
 #pragma unroll 1
         for (int t = e; t < kTilesPerBlock; t += kEpi) {
-          float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          // three independent chains (the hi, mid and lo parts of XS), added in a fixed order
+          float zq[3][4] = {};
           const unsigned char* srow = stage + (t * kTileRows + g) * KG * 2 + 4 * c;
           for (int kk = 0; kk < KG / 8; ++kk) {
             uint32_t av[4];
@@ -371,9 +372,12 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
 #pragma unroll
             for (int part = 0; part < 3; ++part) {
               const uint2 b = zlive ? zl[(kk * 3 + part) * mt * 4] : make_uint2(0u, 0u);
-              mma_bf16_16816_acc(z, av[0], av[1], av[2], av[3], b.x, b.y);
+              mma_bf16_16816_acc(zq[part], av[0], av[1], av[2], av[3], b.x, b.y);
             }
           }
+          float z[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) z[j] = (zq[0][j] + zq[1][j]) + zq[2][j];
           float* zw = zp + (t * kTileRows + g) * rp;
           if (2 * c < mt) {
             zw[2 * c] = z[0];
@@ -391,7 +395,7 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
         __threadfence_block();
         mbar_arrive(&zp_done[buf]);
       }
-      if (!wait_warp(&zp_done[buf], static_cast<uint32_t>(ph), 100u)) break;
+      if (!wait_warp(&zp_done[buf], static_cast<uint32_t>(ph), 0u)) break;
       const int b = static_cast<int>(blockIdx.x) + lb * static_cast<int>(gridDim.x);
       const int n0 = b * kBlockRows + lane;
       for (int m = e; m < mt; m += kEpi) {
@@ -649,8 +653,10 @@ int round16(int v) { return (v + 15) / 16 * 16; }
 bool plan_stream(StreamArgs& a, int mt, int max_smem, int* smem) {
   const int NW = a.NW;
   a.rp = mt == 1 ? 1 : (mt | 1);  // odd: a warp reading one column over 32 rows hits 32 banks
-  static const int kPlans[][3] = {{2, 4, 8}, {2, 4, 6}, {2, 2, 6}, {2, 4, 4}, {2, 2, 4},
-                                  {1, 4, 4}, {2, 2, 3}, {1, 2, 3}, {1, 2, 2}};
+  // {partial buffers, S/ZS stages, tile stages}
+  static const int kPlans[][3] = {{4, 4, 8}, {3, 4, 8}, {2, 4, 8}, {2, 4, 6}, {2, 2, 6},
+                                  {2, 4, 4}, {2, 2, 4}, {1, 4, 4}, {2, 2, 3}, {1, 2, 3},
+                                  {1, 2, 2}};
   for (const auto& pl : kPlans) {
     const int nb = pl[0], nsb = pl[1], ns = pl[2];
     int off = 0;
