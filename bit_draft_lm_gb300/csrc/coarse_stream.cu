@@ -68,6 +68,26 @@ constexpr int kWarpTile = kTileRows * kStrip;  // 1 KB: one warp's part of a til
 __device__ __forceinline__ uint32_t lds_bf16(const unsigned char* p) {
   return *reinterpret_cast<const uint16_t*>(p);
 }
+// Adds one to a shared-memory counter where `pred` holds and returns its previous value (0 where
+// it does not), without a branch: the lanes that skip it do not wait for it.
+__device__ __forceinline__ int atom_inc_if(int* p, bool pred) {
+  int old;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\tmov.u32 %0, 0;\n\t"
+      "@q atom.shared::cta.add.u32 %0, [%1], 1;\n\t}"
+      : "=r"(old)
+      : "r"(smem_addr(p)), "r"(pred ? 1u : 0u)
+      : "memory");
+  return old;
+}
+// One arrival on `bar` where `pred` holds (release at CTA scope), without a branch.
+__device__ __forceinline__ void mbar_arrive_if(uint64_t* bar, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_addr(bar)),
+      "r"(pred ? 1u : 0u)
+      : "memory");
+}
 
 struct StreamArgs {
   const uint16_t* x;  // bf16 [M, K]
@@ -490,25 +510,51 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     const int qa = MT1 ? (2 * c < NQ ? 2 * c : 0) : 0;
     auto s_col = [&](int q) { return q * (RB / G) + strip_byte / G; };
     const int soa = so_g + 2 * s_col(qa), sob = so_g + 2 * s_col(qa + 1 < NQ ? qa + 1 : qa);
-    int s = 0, sph = 0, st = 0, stph = 0, buf = 0, rph = 0;
+    // Ring positions are fixed per block: ns is 4 or 8, so block lb's tiles sit in stages
+    // s0 .. s0 + 3 with s0 = 4 (lb & 1) (ns = 8) or 0 (ns = 4), all of the same phase parity.
+    // The release of a stage is lane 0's predicated counter add; whether this warp was the last
+    // of the NW (and so refills the stage) is looked at one tile later, when the add's result is
+    // long back, by a warp vote: no lane waits on the add, and the warp never diverges for it.
+    int st = 0, stph = 0, buf = 0, rph = 0;
+    int pend_old = 0, pend_s = 0, pend_tau = -1;  // the last release: lane 0's counter value
+    auto refill_if_last = [&]() {
+      if (__any_sync(0xffffffffu, lane == 0 && pend_tau >= 0 && pend_old == NW - 1)) {
+        if (lane == 0) {
+          tcnt[pend_s] = 0;
+          __threadfence_block();
+          const int nxt = pend_tau + ns;
+          if (nxt < ntiles) {
+            fence_proxy_async_smem();  // the stage's reads come before the copy's writes
+            issue_tile(nxt, pend_s);
+          }
+        }
+        __syncwarp();
+      }
+    };
     for (int lb = 0; lb < my_blocks; ++lb) {
       bool ok = wait_warp(&sz_full[st], static_cast<uint32_t>(stph), 0u);
       if (ok && lb >= nb) ok = wait_warp(&red_empty[buf], static_cast<uint32_t>(rph ^ 1), 0u);
       if (!ok) break;
       const unsigned char* stage = sz + st * 2 * sz_half;
       float* rwb = red + buf * NW * red_wstride + warp * red_wstride + g * rp + (MT1 ? 0 : 2 * c);
+      const int s0 = ns == 8 ? 4 * (lb & 1) : 0;
+      const uint32_t tph = static_cast<uint32_t>(ns == 8 ? (lb >> 1) & 1 : lb & 1);
+      const unsigned char* cs0 = ring + s0 * tstage + warp * kWarpTile;
+      bool rdy = mbar_test_wait(&tile_full[s0], tph);
 #pragma unroll
       for (int t = 0; t < kTilesPerBlock; ++t) {
-        if (!wait_warp(&tile_full[s], static_cast<uint32_t>(sph), 0u)) {
+        if (!__all_sync(0xffffffffu, rdy) && !wait_warp(&tile_full[s0 + t], tph, 0u)) {
           ok = false;
           break;
         }
-        const unsigned char* cs = ring + s * tstage + warp * kWarpTile;
+        const unsigned char* cs = cs0 + t * tstage;
         const unsigned char* szs = stage + t * (kTileRows * KG * 2);
         const uint4 wa = *reinterpret_cast<const uint4*>(cs + g * kStrip + 16 * c);
         const uint4 wb = *reinterpret_cast<const uint4*>(cs + (g + 8) * kStrip + 16 * c);
+        // the next tile's stage, tested now so that the answer is back when it is needed
+        if (t + 1 < kTilesPerBlock) rdy = mbar_test_wait(&tile_full[s0 + t + 1], tph);
         const uint32_t ta[4] = {wa.x, wa.y, wa.z, wa.w}, tb[4] = {wb.x, wb.y, wb.z, wb.w};
-        float acc[4];
+        float* rw = rwb + t * kTileRows * rp;
         if (MT1) {
           // one accumulator per scale group q (four independent chains); column q of dq[q] is
           // group q's dot, the other columns are ignored
@@ -540,11 +586,12 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
           float r8 = fmaf(sb8, db3, sa8 * da2);
           r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
           r8 += __shfl_xor_sync(0xffffffffu, r8, 1);
-          acc[0] = r0;
-          acc[2] = r8;
-          acc[1] = acc[3] = 0.0f;
+          // partials in logit units: rows g and g + 8, from lane c = 0
+          const float v0 = r0 * ysc[0], v8 = r8 * ysc[0];
+          if (c == 0) rw[0] = v0;
+          if (c == 0) rw[8] = v8;
         } else {
-          acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
           uint32_t tao[4], tbo[4];  // odd bytes moved down: t >> 8
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -568,52 +615,36 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
             acc[2] = fmaf(sg8, d[2], acc[2]);
             acc[3] = fmaf(sg8, d[3], acc[3]);
           }
+          // partials in logit units, D layout: acc[0..1] = row g, hidden rows 2c, 2c + 1;
+          // acc[2..3] = row g + 8
+          const float v0 = acc[0] * ysc[0], v1 = acc[1] * ysc[1];
+          const float v2 = acc[2] * ysc[0], v3 = acc[3] * ysc[1];
+          const bool lo = 2 * c < mt, hi1 = 2 * c + 1 < mt;
+          if (lo) rw[0] = v0;
+          if (lo) rw[8 * rp] = v2;
+          if (hi1) rw[1] = v1;
+          if (hi1) rw[8 * rp + 1] = v3;
         }
-        // the stage has been read (every lane's loads were consumed above); the last of the NW
-        // warps to release it issues its next tile
+        // the previous release's refill, if this warp was its last arriver
+        refill_if_last();
+        // this stage has been read (every lane's loads were consumed above): release it
         __syncwarp();
-        if (lane == 0) {
-          __threadfence_block();
-          if (atomicAdd(&tcnt[s], 1) == NW - 1) {
-            tcnt[s] = 0;
-            __threadfence_block();
-            const int nxt = kTilesPerBlock * lb + t + ns;
-            if (nxt < ntiles) {
-              fence_proxy_async_smem();  // the stage's reads come before the copy's writes
-              issue_tile(nxt, s);
-            }
-          }
-        }
-        if (++s == ns) { s = 0; sph ^= 1; }
-        // partials in logit units, D layout: acc[0..1] = row g, hidden rows 2c, 2c+1;
-        // acc[2..3] = row g + 8 (MT1: acc[0], acc[2] in lane c = 0)
-        float* rw = rwb + t * kTileRows * rp;
-        if (MT1) {
-          if (c == 0) {
-            rw[0] = acc[0] * ysc[0];
-            rw[8] = acc[2] * ysc[0];
-          }
-        } else {
-          if (2 * c < mt) {
-            rw[0] = acc[0] * ysc[0];
-            rw[8 * rp] = acc[2] * ysc[0];
-          }
-          if (2 * c + 1 < mt) {
-            rw[1] = acc[1] * ysc[1];
-            rw[8 * rp + 1] = acc[3] * ysc[1];
-          }
-        }
+        pend_old = atom_inc_if(&tcnt[s0 + t], lane == 0);
+        pend_s = s0 + t;
+        pend_tau = kTilesPerBlock * lb + t;
       }
       if (!ok) break;
-      // the block's partials are written: hand them to the block's epilogue warp
+      // the block's partials are written: hand them to the epilogue (the arrival releases them)
       __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        mbar_arrive(&red_full[buf]);
-      }
+      mbar_arrive_if(&red_full[buf], lane == 0);
+      // the block's last release is looked at now: a warp about to wait for the epilogue must not
+      // hold back the ring
+      refill_if_last();
+      pend_tau = -1;
       if (++st == nsb) { st = 0; stph ^= 1; }
       if (++buf == nb) { buf = 0; rph ^= 1; }
     }
+    refill_if_last();  // the last release (its next tile, if any, is another warp's to wait for)
   }
   __syncthreads();
   // After an abort, copies may still be in flight: they land before the CTA's shared memory goes
@@ -654,9 +685,9 @@ bool plan_stream(StreamArgs& a, int mt, int max_smem, int* smem) {
   const int NW = a.NW;
   a.rp = mt == 1 ? 1 : (mt | 1);  // odd: a warp reading one column over 32 rows hits 32 banks
   // {partial buffers, S/ZS stages, tile stages}
-  static const int kPlans[][3] = {{4, 4, 8}, {3, 4, 8}, {2, 4, 8}, {2, 4, 6}, {2, 2, 6},
-                                  {2, 4, 4}, {2, 2, 4}, {1, 4, 4}, {2, 2, 3}, {1, 2, 3},
-                                  {1, 2, 2}};
+  // {partial buffers, S/ZS stages, tile stages}; the kernel takes 4 or 8 tile stages
+  static const int kPlans[][3] = {{4, 4, 8}, {3, 4, 8}, {2, 4, 8}, {2, 2, 8}, {1, 4, 8},
+                                  {2, 4, 4}, {2, 2, 4}, {1, 4, 4}, {1, 2, 4}};
   for (const auto& pl : kPlans) {
     const int nb = pl[0], nsb = pl[1], ns = pl[2];
     int off = 0;
