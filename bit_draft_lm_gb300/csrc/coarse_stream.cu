@@ -151,15 +151,17 @@ __global__ void __launch_bounds__(kSMaxThreads, 1)
     *abort_flag = 1;
     set_status(a.status, DH_DEV_WAIT_TIMEOUT);
   };
-  // Bounded wait of one thread: tests spaced by `sleep_ns` of __nanosleep (0: a plain spin),
-  // the abort flag and the clock looked at every 64 tests. False once the launch is aborted (its
+  // Bounded wait of one thread: tests spaced by `sleep_ns` of __nanosleep (the abort flag and
+  // the clock looked at every 64 tests), or with sleep_ns == 0 suspended waits (try_wait) with the
+  // flag and the clock looked at after each. False once the launch is aborted (its
   // own timeout or another thread's).
   auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t sleep_ns) -> bool {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-      if (mbar_test_wait(bar, parity)) return true;
+      // sleep_ns == 0: the hardware's suspended wait (woken by the phase's completion)
+      if (sleep_ns ? mbar_test_wait(bar, parity) : mbar_try_wait_hw(bar, parity)) return true;
       if (sleep_ns) __nanosleep(sleep_ns);
-      if ((it & 63u) == 0u) {
+      if (sleep_ns == 0u || (it & 63u) == 0u) {
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
           fail();
