@@ -61,12 +61,6 @@ cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, 
   // many hidden rows of an int2 head: one tensor-core pass instead of several warp-MMA passes
   if (cc.scratch != nullptr && coarse_wide_supports(cc))
     return launch_coarse_wide(cc, cc.scratch, num_sms, max_smem, s);
-  // int2 heads: the warp-specialised streaming kernel (tensor-map tiles); the warp-MMA kernel
-  // below takes the int4 head and any shape the streaming kernel's plan does not fit
-  if (coarse_stream_supports(cc)) {
-    const cudaError_t e = launch_coarse_stream(cc, num_sms, max_smem, s);
-    if (e != cudaErrorNotSupported) return e;
-  }
   CoarseArgs a{};
   a.x = static_cast<const uint16_t*>(cc.x);
   a.M = static_cast<int>(cc.M);

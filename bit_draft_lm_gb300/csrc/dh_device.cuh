@@ -81,19 +81,6 @@ __device__ __forceinline__ bool mbar_try_wait_ns(uint64_t* bar, uint32_t parity,
       : "memory");
   return ok != 0;
 }
-// One potentially blocking test of the phase with the hardware's own suspend time: the thread is
-// suspended (it takes no issue slots) until the phase completes or that time runs out.
-__device__ __forceinline__ bool mbar_try_wait_hw(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Non-blocking test of the phase.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

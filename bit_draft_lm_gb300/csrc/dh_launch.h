@@ -51,10 +51,6 @@ cudaError_t launch_quantize_pack(int bits, const void* W, int64_t N, int64_t K, 
                                  const float* row_scale = nullptr);
 // cudaErrorInvalidValue: the shape does not fit the kernel's shared-memory plan.
 cudaError_t launch_coarse_topk(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s);
-// The warp-specialised streaming pass of int2 heads (coarse_stream.cu): one tensor-map copy per
-// 16-row tile, passes of up to 8 hidden rows. cudaErrorNotSupported: use the other kernels.
-bool coarse_stream_supports(const CoarseCall& cc);
-cudaError_t launch_coarse_stream(const CoarseCall& cc, int num_sms, int max_smem, cudaStream_t s);
 // The tensor-core (tcgen05) pass of int2 heads for more than kWideMinRows hidden rows, up to
 // kWideMaxRows per pass (coarse_tc.cu). Its scratch (the hidden states laid out as the MMA
 // operand, their group sums and scales) lives in the caller's workspace.
