@@ -18,16 +18,17 @@
 //  * Persistent grid, one CTA per SM, 128-row tiles (the MMA's M = TMEM lanes). Warp 0 streams
 //    the packed rows through a ring of 128 x 128-byte stages with 2-D tensor-map copies (TMA,
 //    128-byte swizzle); warp 2 streams the B units through a second ring with bulk copies.
-//  * 4 dequantising warps: the thread of TMEM lane r owns row r. A 16-byte chunk of its row
-//    (16 byte positions x 4 planes) becomes 32 registers of f16 pairs with one AND each (the
-//    odd bytes come down by one shift per word), written to a TMEM A stage by one tcgen05.st;
-//    plane p's 16 codes are the stage's columns 8p .. 8p + 7.
-//  * Warp 1 (one thread) issues the MMAs plane by plane within each scale group: for plane p,
-//    the group's chunks accumulate into one D slot (128 x N fp32), which is then handed to the
-//    fold warps while the next plane accumulates into the other slot. So the page's
-//    per-group scale is applied to the accumulator, never to the weight tile:
-//    acc += S[n, g] * D_g. The zero-point part sum_g (S - ZS) XS_g (the page's
-//    S (XS + sum x v / 4) - ZS XS rearranged) is a per-row dot with the group sums.
+//  * 8 dequantising warps, two per TMEM lane quadrant (even and odd chunks of a group); the
+//    thread of TMEM lane r owns row r. A 16-byte chunk of its row (16 byte positions x 4 planes)
+//    gives, for one plane pair, 16 registers of f16 pairs with one AND each (the odd bytes come
+//    down by one shift per word), written to a TMEM A stage by one tcgen05.st: plane 2h + q's 16
+//    codes are the stage's columns 8q .. 8q + 7.
+//  * Two MMA-issuing threads (warps 1 and 3), one per plane of a pair, so that two independent
+//    accumulation chains keep the tensor pipe busy: for plane p of scale group J the group's
+//    chunks accumulate into one D slot (128 x N fp32); four D slots let one plane pair be folded
+//    while the next accumulates. So the page's per-group scale is applied to the accumulator,
+//    never to the weight tile: acc += S[n, g] * D_g. The zero-point part sum_g (S - ZS) XS_g
+//    (the page's S (XS + sum x v / 4) - ZS XS rearranged) is a per-row dot with the group sums.
 //  * 8 fold warps (two per TMEM lane quadrant, half of the columns each; thread = row) add
 //    S_g D_g and the zero-point part (S_g - ZS_g) XS_g of every slot into registers, then hand
 //    the tile's keys to 4 selection warps, which pick the top-KCAND of each 64-row block per
@@ -51,11 +52,19 @@ namespace dh {
 constexpr int kWRows = 128;        // vocab rows per tile (MMA M, TMEM lanes)
 constexpr int kWStageBytes = 128;  // packed bytes of a row per ring stage (8 chunks)
 constexpr int kWStageSmem = kWRows * kWStageBytes;
-constexpr int kWWarps = 19;  // producer, MMA, B producer, 4 dequantising, 8 fold, 4 selection
+constexpr int kWDeqWarps = 8;   // dequantising: two per TMEM lane quadrant
+constexpr int kWFoldWarps = 8;  // fold: two per TMEM lane quadrant
+constexpr int kWSelWarps = 4;   // block top-KCAND selection
+// packed producer, MMA issuer A, B producer, MMA issuer B, then the dequantising, fold and
+// selection warps
+constexpr int kWDeq0 = 4;                         // first dequantising warp
+constexpr int kWFold0 = kWDeq0 + kWDeqWarps;      // first fold warp
+constexpr int kWSel0 = kWFold0 + kWFoldWarps;     // first selection warp
+constexpr int kWWarps = kWSel0 + kWSelWarps;
 constexpr int kWThreads = kWWarps * 32;
-constexpr int kWMaxNP = 8;  // packed ring stages at most
-constexpr int kWMaxNB = 4;  // B ring units at most
-constexpr int kWMaxNA = 12;
+constexpr int kWMaxNP = 8;   // packed ring stages at most
+constexpr int kWMaxNB = 4;   // B ring units at most
+constexpr int kWMaxNA = 28;  // A stages at most (16 TMEM columns each)
 constexpr int kWTmemCols = 512;
 constexpr int kWPrepThreads = 256;
 
@@ -160,14 +169,16 @@ __global__ void __launch_bounds__(kWThreads, 1)
     coarse_wide_kernel(const __grid_constant__ CUtensorMap tmap, const WideArgs a) {
   constexpr int P = 4;           // int2 planes
   constexpr int CPJ = G / 16;    // chunks per scale group
-  constexpr int ACOLS = 8 * P;   // TMEM columns of one A stage
-  // A stages, an even number: they are released in pairs (chunks 2q, 2q + 1), one commit each
-  constexpr int NA = ((kWTmemCols - 2 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
-                                                                  : (kWTmemCols - 2 * NCOL) / ACOLS) &
-                     ~1;
+  constexpr int ACOLS = 16;      // TMEM columns of one A stage: one chunk, two planes
+  // Four D slots (two per plane pair, double-buffered by pair) at columns 0 .. 4 NCOL, then the
+  // A stages (chunk, plane pair), an even number: they are released in pairs (chunks 2q, 2q + 1)
+  constexpr int NAS = ((kWTmemCols - 4 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
+                                                                   : (kWTmemCols - 4 * NCOL) / ACOLS) &
+                      ~1;
   constexpr int PITCH = NCOL + 1;  // words per row of the key buffer (odd: no bank conflicts)
+  constexpr int HC = NCOL / 2;     // D columns of one fold warp
   static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 80, "MMA N");
-  static_assert(NA >= CPJ + 2, "TMEM budget: a group's chunks plus one spare pair");
+  static_assert(NAS >= CPJ + 2, "TMEM budget: a group's chunks plus one spare pair");
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte alignment for the 128-byte swizzle of the packed ring
   unsigned char* sm = sm_raw + ((1024u - (smem_addr(sm_raw) & 1023u)) & 1023u);
@@ -180,8 +191,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
   uint64_t* bempty = bfull + kWMaxNB;   // [kWMaxNB] B unit's D slot read (its MMAs are done)
   uint64_t* afull = bempty + kWMaxNB;   // [kWMaxNA] A stage written
   uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA / 2] A stage pair's MMAs done
-  uint64_t* dfull = aempty + kWMaxNA;   // [2] D slot complete
-  uint64_t* dempty = dfull + 2;         // [2] D slot read by the fold warps
+  uint64_t* dfull = aempty + kWMaxNA;   // [2] D slot pair complete
+  uint64_t* dempty = dfull + 2;         // [2] D slot pair read by the fold warps
   uint64_t* mma_done = dempty + 2;      // every MMA of the CTA complete
   uint64_t* keys_ready = mma_done + 1;  // a tile's keys written by the fold warps
   uint64_t* keys_free = mma_done + 2;   // ... and consumed by the selection warps
@@ -197,23 +208,23 @@ __global__ void __launch_bounds__(kWThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWMaxNP; ++i) {
       mbar_init(&pfull[i], 1u);
-      mbar_init(&pempty[i], 4u);
+      mbar_init(&pempty[i], static_cast<uint32_t>(kWDeqWarps));
     }
     for (int i = 0; i < kWMaxNB; ++i) {
       mbar_init(&bfull[i], 1u);
-      mbar_init(&bempty[i], 8u);  // the 8 fold warps
+      mbar_init(&bempty[i], static_cast<uint32_t>(kWFoldWarps));
     }
     for (int i = 0; i < kWMaxNA; ++i) {
-      mbar_init(&afull[i], 4u);
-      mbar_init(&aempty[i], 1u);
+      mbar_init(&afull[i], 4u);  // the 4 quadrant warps of the stage's chunk parity
+      mbar_init(&aempty[i], 2u);  // one commit from each MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&dfull[i], 1u);
-      mbar_init(&dempty[i], 8u);  // the 8 fold warps
+      mbar_init(&dfull[i], 2u);  // one commit from each MMA issuer
+      mbar_init(&dempty[i], static_cast<uint32_t>(kWFoldWarps));
     }
-    mbar_init(mma_done, 1u);
-    mbar_init(keys_ready, 8u);
-    mbar_init(keys_free, 4u);
+    mbar_init(mma_done, 2u);
+    mbar_init(keys_ready, static_cast<uint32_t>(kWFoldWarps));
+    mbar_init(keys_free, static_cast<uint32_t>(kWSelWarps));
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_map(&tmap);
@@ -223,12 +234,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_base = tmem + 2 * NCOL;  // column of A stage 0 (D slots at 0 and NCOL)
+  const uint32_t a_base = tmem + 4 * NCOL;  // column of A stage 0 (D slots at k NCOL, k < 4)
 
-  // Bounded wait on one phase of an mbarrier. Returns at once (false) once the launch is
-  // aborted; a wait that runs out aborts it. Callers go on either way (uniform control flow).
+  // Bounded wait on one phase of an mbarrier: one test first (the common case costs one
+  // instruction and no clock read), then suspended waits. Returns at once (false) once the launch
+  // is aborted; a wait that runs out aborts it. Callers go on either way (uniform control flow).
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
       if (*abort_flag) return false;
@@ -243,6 +255,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
   auto tile_of = [&](int lt) {
     return static_cast<int>(blockIdx.x) + lt * static_cast<int>(gridDim.x);
   };
+  // ring position (slot, phase parity) advanced by one without a division
+  auto advance = [](int& slot, uint32_t& ph, int n) {
+    if (++slot == n) {
+      slot = 0;
+      ph ^= 1u;
+    }
+  };
 
   int issued = 0, issued_b = 0;  // copies issued by warp 0 / warp 2 (lane 0)
   if (warp == 0) {
@@ -253,14 +272,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
       for (int s = 0; s < np && s < total_stages; ++s)
         tma_prefetch_l2_2d(&tmap, (s % a.NS) * kWStageBytes, tile_of(s / a.NS) * kWRows);
       grid_dependency_wait();
+      int slot = 0, lt = 0, s = 0;
+      uint32_t ph = 0u;
       for (; issued < total_stages; ++issued) {
-        const int slot = issued % np;
-        if (issued >= np) wait_bar(&pempty[slot], static_cast<uint32_t>(issued / np - 1) & 1u);
+        if (issued >= np) wait_bar(&pempty[slot], ph ^ 1u);
         if (*abort_flag) break;
-        const int lt = issued / a.NS, s = issued - lt * a.NS;
         mbar_arrive_expect_tx(&pfull[slot], static_cast<uint32_t>(kWStageSmem));
         tma_load_2d(sm + slot * kWStageSmem, &tmap, s * kWStageBytes, tile_of(lt) * kWRows,
                     &pfull[slot]);
+        advance(slot, ph, np);
+        if (++s == a.NS) {
+          s = 0;
+          ++lt;
+        }
       }
     }
     __syncwarp();
@@ -269,46 +293,61 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (lane == 0) {
       grid_dependency_wait();
       const int total_units = my_tiles * units_per_tile;
+      int slot = 0, unit = 0;
+      uint32_t ph = 0u;
       for (; issued_b < total_units; ++issued_b) {
-        const int slot = issued_b % nbu;
-        if (issued_b >= nbu)
-          wait_bar(&bempty[slot], static_cast<uint32_t>(issued_b / nbu - 1) & 1u);
+        if (issued_b >= nbu) wait_bar(&bempty[slot], ph ^ 1u);
         if (*abort_flag) break;
-        const int unit = issued_b % units_per_tile;
         mbar_arrive_expect_tx(&bfull[slot], static_cast<uint32_t>(a.unit_bytes));
         bulk_g2s(sm + a.off_bring + slot * a.unit_bytes,
                  a.bbuf + static_cast<int64_t>(unit) * a.unit_bytes,
                  static_cast<uint32_t>(a.unit_bytes), &bfull[slot]);
+        advance(slot, ph, nbu);
+        if (++unit == units_per_tile) unit = 0;
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---- MMA issue: per (group J, plane p) the group's chunks into one D slot -----------------
+  } else if (warp == 1 || warp == 3) {
+    // ---- MMA issue, two threads (one tcgen05.mma stream each, so that the tensor pipe overlaps
+    // them): issuer pl takes plane 2h + pl of every (group J, plane pair h), the group's chunks
+    // into D slot 2k + pl (k the pair's parity), A from the pair's stages, which both issuers
+    // release two by two. Descriptors and ring positions move by additions only.
+    const int pl = warp == 3 ? 1 : 0;
     if (lane == 0) {
       const uint32_t idesc = tc_idesc_f16(kWRows, NCOL);
-      const uint32_t b_ring = smem_addr(sm + a.off_bring);
-      int gslot = 0, gu = 0;
+      const uint64_t bdesc0 = tc_sdesc(smem_addr(sm + a.off_bring), NCOL * 16, 128u);
+      int bslot = pl;  // this issuer's B units: every other unit of the ring (nbu is even)
+      uint32_t bph = 0u;
+      int as = 0;
+      uint32_t aph = 0u;
+      int pr = 0;  // pairs issued; D slot 2 (pr & 1) + pl
       for (int lt = 0; lt < my_tiles; ++lt) {
         for (int J = 0; J < a.NJ; ++J) {
-          for (int p = 0; p < P; ++p, ++gslot, ++gu) {
-            const int bslot = gu % nbu, dbuf = gslot & 1;
-            wait_bar(&bfull[bslot], static_cast<uint32_t>(gu / nbu) & 1u);
-            if (gslot >= 2) wait_bar(&dempty[dbuf], static_cast<uint32_t>((gslot >> 1) - 1) & 1u);
+          for (int h = 0; h < 2; ++h, ++pr) {
+            const int k = pr & 1;
+            wait_bar(&bfull[bslot], bph);
+            if (pr >= 2) wait_bar(&dempty[k], static_cast<uint32_t>((pr >> 1) - 1) & 1u);
             tc_fence_after();
-            const uint32_t unit = b_ring + bslot * a.unit_bytes;
+            const uint64_t bd = bdesc0 + static_cast<uint64_t>((bslot * a.unit_bytes) >> 4);
+            const uint32_t d = tmem + (2 * k + pl) * NCOL;
+#pragma unroll 2
             for (int cj = 0; cj < CPJ; ++cj) {
-              const int ga = lt * a.NC + J * CPJ + cj, aslot = ga % NA;
-              if (p == 0) {
-                wait_bar(&afull[aslot], static_cast<uint32_t>(ga / NA) & 1u);
-                tc_fence_after();
-              }
-              const uint64_t bdesc = tc_sdesc(unit + cj * (2 * NCOL * 16), NCOL * 16, 128u);
-              tc_mma_f16_ts(tmem + dbuf * NCOL, a_base + aslot * ACOLS + 8 * p, bdesc, idesc,
+              wait_bar(&afull[as], aph);
+              tc_fence_after();
+              tc_mma_f16_ts(d, a_base + as * ACOLS + 8 * pl,
+                            bd + static_cast<uint64_t>((cj * 2 * NCOL * 16) >> 4), idesc,
                             cj != 0);
-              if (p == P - 1 && (cj & 1)) tc_commit(&aempty[aslot >> 1]);
+              if (cj & 1) tc_commit(&aempty[as >> 1]);
+              advance(as, aph, NAS);
             }
-            // one commit per unit: the fold warps that read the D slot also release the B unit
-            tc_commit(&dfull[dbuf]);
+            // one commit per pair and issuer: the fold warps that read the two slots release the
+            // B units
+            tc_commit(&dfull[k]);
+            bslot += 2;
+            if (bslot >= nbu) {
+              bslot -= nbu;
+              bph ^= 1u;
+            }
           }
         }
       }
@@ -316,209 +355,245 @@ __global__ void __launch_bounds__(kWThreads, 1)
       mbar_wait_bounded(mma_done, 0u);  // also after an abort: no MMA may outlive the TMEM
     }
     __syncwarp();
-  } else if (warp < 7) {
-    // ---- dequantisation: every chunk of every tile, one thread per row --------------------------
+  } else if (warp >= kWDeq0 && warp < kWFold0) {
+    // ---- dequantisation: eight warps, two per TMEM lane quadrant (one for the even chunks of a
+    // group, one for the odd), one thread per row. A stage holds one chunk's two planes of a pair
+    // (16 columns): planes 2h, 2h + 1 of 16 byte positions as f16 pairs (one AND each).
+    const int sub = (warp - kWDeq0) >> 2;  // chunk parity of this warp
     const int row = (warp & 3) * 32 + lane;
     const uint32_t my_a = a_base + tmem_lane_base(warp);
     const int sw = row & 7;
-    int gs_cur = -1;
+    int ps = 0;  // packed ring slot of the current stage
+    uint32_t pph = 0u;
+    int as0 = 0;  // A ring slot of the current pair's chunk 0
+    uint32_t aph0 = 0u;
+    int a_issued0 = 0;  // A stages the whole pass has begun before the current pair
     for (int lt = 0; lt < my_tiles; ++lt) {
-      for (int c = 0; c < a.NC; ++c) {
-        const int ga = lt * a.NC + c, gs = lt * a.NS + (c >> 3);
-        if (gs != gs_cur) {
-          if (gs_cur >= 0) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pempty[gs_cur % np]);
-          }
-          wait_bar(&pfull[gs % np], static_cast<uint32_t>(gs / np) & 1u);
-          __syncwarp();
-          gs_cur = gs;
-        }
-        const int slot = ga % NA;
-        if (ga >= NA) {
-          wait_bar(&aempty[slot >> 1], static_cast<uint32_t>(ga / NA - 1) & 1u);
+      for (int J = 0; J < a.NJ; ++J) {
+        const int c0 = J * CPJ;  // the group's first chunk within the tile
+        if ((c0 & 7) == 0) {     // the group starts a packed stage (8 chunks)
+          wait_bar(&pfull[ps], pph);
           __syncwarp();
         }
-        tc_fence_after();
-        const uint4 w4 = *reinterpret_cast<const uint4*>(
-            sm + (gs % np) * kWStageSmem + row * kWStageBytes + (((c & 7) ^ sw) << 4));
-        const uint32_t t[4] = {w4.x, w4.y, w4.z, w4.w};
-        uint32_t r[32];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t te = t[w], to = t[w] >> 8;
-#pragma unroll
-          for (int p = 0; p < P; ++p) {
-            r[8 * p + 2 * w] = te & (0x00030003u << (2 * p));
-            r[8 * p + 2 * w + 1] = to & (0x00030003u << (2 * p));
-          }
-        }
-        tmem_st_x32(my_a + slot * ACOLS, r);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[slot]);
-      }
-    }
-    if (gs_cur >= 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pempty[gs_cur % np]);
-    }
-  } else {
-    // ---- fold: two warps per TMEM lane quadrant, each NCOL/2 columns of its 32 rows ----------------
-    if (warp < 15) {
-      constexpr int HC = NCOL / 2;  // columns of this warp
-      const int fw = warp - 7;      // 0..7
-      const int half = fw >> 2;
-      const int row = (warp & 3) * 32 + lane;
-      const int col0 = half * HC;
-      const uint32_t my_d = tmem + tmem_lane_base(warp) + col0;
-      unsigned char* s_row = sm + a.off_sz + row * a.szp;  // this row's S ...
-      unsigned char* z_row = s_row + kWRows * a.szp;       // ... and ZS
-      uint32_t* keys = reinterpret_cast<uint32_t*>(sm + a.off_keys);  // [128][PITCH]
-      float* xsd = reinterpret_cast<float*>(sm + a.off_xs);           // [KG][NCOL]
-      int* ew_s = reinterpret_cast<int*>(sm + a.off_ew);              // [NCOL]
-      // the half-0 warp copies the row's S, the half-1 warp its ZS; a barrier of the fold warps
-      // then shares them
-      auto load_sz = [&](int lt) {
-        const int n = tile_of(lt) * kWRows + row;
-        const bool valid = n < a.N;
-        const int64_t off = static_cast<int64_t>(valid ? n : 0) * a.KG;
-        const uint16_t* src = (half ? a.ZS : a.S) + off;
-        unsigned char* dst = half ? z_row : s_row;
-        for (int i = 0; i < a.KG / 8; ++i) w_cp_async16(smem_addr(dst + 16 * i), src + 8 * i, valid);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-      };
-      // the first tile's scales into L2 while the preceding kernel may still run (only L2
-      // before the wait, as for the packed rows); the copies into shared memory follow it
-      if (my_tiles > 0) {
-        const int n = tile_of(0) * kWRows + row;
-        if (n < a.N)
-          prefetch_l2_bulk((half ? a.ZS : a.S) + static_cast<int64_t>(n) * a.KG,
-                           static_cast<uint32_t>(a.KG * 2));
-      }
-      // the prep kernel's group sums and exponents (the outputs are written after this wait
-      // too): XS in the units of the D slots, 2^24 / (2^(15 - E_m) 4) = 2^(E_m + 7), as
-      // xsd[g][m] = XS[m][g] 2^-(E_m + 7) (a power of two: exact)
-      grid_dependency_wait();
-      if (my_tiles > 0) load_sz(0);
-      const int ftid = fw * 32 + lane;
-      if (ftid < NCOL) ew_s[ftid] = a.ew[ftid];
-      for (int i = ftid; i < NCOL * a.KG; i += 256) {
-        const int m = i / a.KG, gi = i - m * a.KG;
-        xsd[gi * NCOL + m] = a.xs[i] * w_pow2(-(a.ew[m] + 7));
-      }
-      named_bar_sync(2, 256);
-      int gslot = 0;
-      for (int lt = 0; lt < my_tiles; ++lt) {
-        const int n = tile_of(lt) * kWRows + row;
-        const bool valid = n < a.N;
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        named_bar_sync(2, 256);  // both halves' copies of the tile's S and ZS rows have landed
-        float acc[HC];
-#pragma unroll
-        for (int m = 0; m < HC; ++m) acc[m] = 0.0f;
-        // the tile's D slots, in the order the MMAs complete them: (group J, plane p); each adds
-        // S_g D_g and the zero-point part (S_g - ZS_g) XS_g
-        for (int J = 0; J < a.NJ; ++J) {
-          for (int p = 0; p < P; ++p, ++gslot) {
-            const int dbuf = gslot & 1, gi = p * a.NJ + J;
-            wait_bar(&dfull[dbuf], static_cast<uint32_t>(gslot >> 1) & 1u);
-            __syncwarp();
-            tc_fence_after();
-            const float sg = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(s_row + 2 * gi));
-            const float zg = sg - bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(z_row + 2 * gi));
-            const float* xg = xsd + gi * NCOL + col0;
-#pragma unroll
-            for (int q = 0; q < HC; q += 8) {
-              uint32_t d[8];
-              tmem_ld<8>(my_d + dbuf * NCOL + q, d);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                acc[q + i] = fmaf(sg, __uint_as_float(d[i]), fmaf(zg, xg[q + i], acc[q + i]));
+        const unsigned char* prow = sm + ps * kWStageSmem + row * kWStageBytes;
+        for (int h = 0; h < 2; ++h) {
+          for (int cj = sub; cj < CPJ; cj += 2) {
+            int as = as0 + cj;
+            uint32_t aph = aph0;
+            if (as >= NAS) {
+              as -= NAS;
+              aph ^= 1u;
             }
+            if (a_issued0 + cj >= NAS) {  // the stage's previous MMAs are done
+              wait_bar(&aempty[as >> 1], aph ^ 1u);
+              __syncwarp();
+            }
+            tc_fence_after();
+            const int c = c0 + cj;
+            const uint4 w4 =
+                *reinterpret_cast<const uint4*>(prow + ((((c & 7) ^ sw)) << 4));
+            const uint32_t t[4] = {w4.x, w4.y, w4.z, w4.w};
+            uint32_t r[16];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t te = t[w], to = t[w] >> 8;
+#pragma unroll
+              for (int pp = 0; pp < 2; ++pp) {
+                const uint32_t mk = 0x00030003u << (2 * (2 * h + pp));
+                r[8 * pp + 2 * w] = te & mk;
+                r[8 * pp + 2 * w + 1] = to & mk;
+              }
+            }
+            tmem_st_x16(my_a + as * ACOLS, r);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(&dempty[dbuf]);
-              mbar_arrive(&bempty[gslot % nbu]);  // the slot's MMAs, and so its B unit, are done
-            }
+            if (lane == 0) mbar_arrive(&afull[as]);
+          }
+          as0 += CPJ;
+          a_issued0 += CPJ;
+          if (as0 >= NAS) {
+            as0 -= NAS;
+            aph0 ^= 1u;
           }
         }
-        named_bar_sync(2, 256);  // both halves are done with the tile's S and ZS rows
-        if (lt + 1 < my_tiles) load_sz(lt + 1);
-#pragma unroll
-        for (int m = 0; m < HC; ++m) acc[m] *= w_pow2(ew_s[col0 + m] + 7);  // logit units
-        if (a.y != nullptr && valid) {
-#pragma unroll
-          for (int m = 0; m < HC; ++m)
-            if (col0 + m < a.R)
-              a.y[static_cast<int64_t>(a.m0 + col0 + m) * a.N + n] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+        if (((c0 + CPJ) & 7) == 0) {  // the packed stage's last group: release it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pempty[ps]);
+          advance(ps, pph, np);
         }
-        // hand the keys to the selection warps (a single buffer: wait until they are done with
-        // the previous tile's)
-        if (lt > 0) wait_bar(keys_free, static_cast<uint32_t>(lt - 1) & 1u);
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < HC; ++m)
-          keys[row * PITCH + col0 + m] = valid ? order_key(acc[m]) : 0u;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(keys_ready);
       }
-    } else {
-      // ---- selection: block top-KCAND of every (64-row block, hidden row) of a tile -----------
-      grid_dependency_wait();  // the outputs
-      const int sw4 = warp - 15;  // 0..3
-      const uint32_t* keys = reinterpret_cast<const uint32_t*>(sm + a.off_keys);
-      for (int lt = 0; lt < my_tiles; ++lt) {
-        const int tile = tile_of(lt);
-        wait_bar(keys_ready, static_cast<uint32_t>(lt) & 1u);
-        __syncwarp();
-        // job j = (64-row block j / R of the tile, hidden row j % R)
-        for (int j = sw4; j < 2 * a.R; j += 4) {
-          const int blk = j / a.R, m = j - blk * a.R;
-          const int b = tile * 2 + blk;
-          if (b >= a.nblk) continue;
-          const uint32_t* kc = keys + 64 * blk * PITCH + m;
-          uint32_t k0 = kc[lane * PITCH], k1 = kc[(lane + 32) * PITCH];
-          uint32_t key_lo = 0u, row_lo = 64u, key_hi = 0u, row_hi = 64u;  // slots lane, lane + 32
-          for (int r = 0; r < a.kcand; ++r) {
-            const bool first = k0 >= k1;
-            const uint32_t bk = first ? k0 : k1;
-            const uint32_t brow =
-                first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
-            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-            const uint32_t rwin = __reduce_min_sync(0xffffffffu, bk == kmax ? brow : 64u);
-            if (kmax != 0u && lane == static_cast<int>(rwin & 31u)) {
-              if (rwin < 32u) k0 = 0u; else k1 = 0u;
-            }
-            if (lane == (r & 31)) {
-              if (r < 32) {
-                key_lo = kmax;
-                row_lo = kmax ? rwin : 64u;
-              } else {
-                key_hi = kmax;
-                row_hi = kmax ? rwin : 64u;
+    }
+  } else if (warp >= kWFold0 && warp < kWSel0) {
+    // ---- fold: two warps per TMEM lane quadrant, each NCOL/2 columns of its 32 rows ------------
+    const int fw = warp - kWFold0;  // 0..7
+    const int half = fw >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const int col0 = half * HC;
+    const uint32_t my_d = tmem + tmem_lane_base(warp) + col0;
+    unsigned char* s_row = sm + a.off_sz + row * a.szp;  // this row's S ...
+    unsigned char* z_row = s_row + kWRows * a.szp;       // ... and ZS
+    uint32_t* keys = reinterpret_cast<uint32_t*>(sm + a.off_keys);  // [128][PITCH]
+    float* xsd = reinterpret_cast<float*>(sm + a.off_xs);           // [KG][NCOL]
+    int* ew_s = reinterpret_cast<int*>(sm + a.off_ew);              // [NCOL]
+    // the half-0 warp copies the row's S, the half-1 warp its ZS; a barrier of the fold warps
+    // then shares them
+    auto load_sz = [&](int lt) {
+      const int n = tile_of(lt) * kWRows + row;
+      const bool valid = n < a.N;
+      const int64_t off = static_cast<int64_t>(valid ? n : 0) * a.KG;
+      const uint16_t* src = (half ? a.ZS : a.S) + off;
+      unsigned char* dst = half ? z_row : s_row;
+      for (int i = 0; i < a.KG / 8; ++i) w_cp_async16(smem_addr(dst + 16 * i), src + 8 * i, valid);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    // the first tile's scales into L2 while the preceding kernel may still run (only L2
+    // before the wait, as for the packed rows); the copies into shared memory follow it
+    if (my_tiles > 0) {
+      const int n = tile_of(0) * kWRows + row;
+      if (n < a.N)
+        prefetch_l2_bulk((half ? a.ZS : a.S) + static_cast<int64_t>(n) * a.KG,
+                         static_cast<uint32_t>(a.KG * 2));
+    }
+    // the prep kernel's group sums and exponents (the outputs are written after this wait
+    // too): XS in the units of the D slots, 2^24 / (2^(15 - E_m) 4) = 2^(E_m + 7), as
+    // xsd[g][m] = XS[m][g] 2^-(E_m + 7) (a power of two: exact)
+    grid_dependency_wait();
+    if (my_tiles > 0) load_sz(0);
+    const int ftid = fw * 32 + lane;
+    if (ftid < NCOL) ew_s[ftid] = a.ew[ftid];
+    for (int i = ftid; i < NCOL * a.KG; i += kWFoldWarps * 32) {
+      const int m = i / a.KG, gi = i - m * a.KG;
+      xsd[gi * NCOL + m] = a.xs[i] * w_pow2(-(a.ew[m] + 7));
+    }
+    named_bar_sync(2, kWFoldWarps * 32);
+    int gslot = 0, bslot = 0;
+    uint32_t bph = 0u;
+    constexpr int kBatch = 24;  // D columns loaded per wait (three 8-column loads)
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      const int n = tile_of(lt) * kWRows + row;
+      const bool valid = n < a.N;
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      named_bar_sync(2, kWFoldWarps * 32);  // both halves' copies of the tile's S, ZS landed
+      float acc[HC];
+#pragma unroll
+      for (int m = 0; m < HC; ++m) acc[m] = 0.0f;
+      // the tile's D slots, in the order the MMAs complete them: (group J, plane p); each adds
+      // S_g D_g and the zero-point part (S_g - ZS_g) XS_g
+      for (int J = 0; J < a.NJ; ++J) {
+        for (int p = 0; p < P; ++p) {
+          // pair pr = gslot of plane p: planes 2h, 2h + 1 complete together in slots 2k, 2k + 1
+          const int k = gslot & 1, gi = p * a.NJ + J, dbuf = 2 * k + (p & 1);
+          if ((p & 1) == 0) {
+            wait_bar(&dfull[k], static_cast<uint32_t>(gslot >> 1) & 1u);
+            __syncwarp();
+            tc_fence_after();
+          }
+          const float sg = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(s_row + 2 * gi));
+          const float zg = sg - bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(z_row + 2 * gi));
+          const float4* xg4 = reinterpret_cast<const float4*>(xsd + gi * NCOL + col0);
+#pragma unroll
+          for (int q0 = 0; q0 < HC; q0 += kBatch) {
+            constexpr int kB = kBatch;
+            uint32_t d[kB];
+#pragma unroll
+            for (int q = 0; q < kB; q += 8)
+              if (q0 + q < HC) tmem_ld<8>(my_d + dbuf * NCOL + q0 + q, d + q);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < kB; q += 4) {
+              if (q0 + q < HC) {
+                const float4 x4 = xg4[(q0 + q) >> 2];
+                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  acc[q0 + q + i] =
+                      fmaf(sg, __uint_as_float(d[q + i]), fmaf(zg, xv[i], acc[q0 + q + i]));
               }
             }
           }
-          const int64_t obase = static_cast<int64_t>(a.m0 + m) * a.nblk * a.kcand +
-                                static_cast<int64_t>(b) * a.kcand;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bempty[bslot]);  // the slot's MMAs, so its B unit, are done
+          advance(bslot, bph, nbu);
+          if (p & 1) {  // both slots of the pair are read
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[k]);
+            ++gslot;
+          }
+        }
+      }
+      named_bar_sync(2, kWFoldWarps * 32);  // both halves are done with the tile's S and ZS rows
+      if (lt + 1 < my_tiles) load_sz(lt + 1);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int slot = lane + 32 * h;
-            const uint32_t kk = h ? key_hi : key_lo, rr = h ? row_hi : row_lo;
-            if (slot < a.kcand) {
-              a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
-              a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
+      for (int m = 0; m < HC; ++m) acc[m] *= w_pow2(ew_s[col0 + m] + 7);  // logit units
+      if (a.y != nullptr && valid) {
+#pragma unroll
+        for (int m = 0; m < HC; ++m)
+          if (col0 + m < a.R)
+            a.y[static_cast<int64_t>(a.m0 + col0 + m) * a.N + n] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+      }
+      // hand the keys to the selection warps (a single buffer: wait until they are done with
+      // the previous tile's)
+      if (lt > 0) wait_bar(keys_free, static_cast<uint32_t>(lt - 1) & 1u);
+      __syncwarp();
+#pragma unroll
+      for (int m = 0; m < HC; ++m) keys[row * PITCH + col0 + m] = valid ? order_key(acc[m]) : 0u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(keys_ready);
+    }
+  } else {
+    // ---- selection: block top-KCAND of every (64-row block, hidden row) of a tile -------------
+    grid_dependency_wait();  // the outputs
+    const int sw4 = warp - kWSel0;  // 0 .. kWSelWarps - 1
+    const uint32_t* keys = reinterpret_cast<const uint32_t*>(sm + a.off_keys);
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      const int tile = tile_of(lt);
+      wait_bar(keys_ready, static_cast<uint32_t>(lt) & 1u);
+      __syncwarp();
+      // job j = (64-row block j / R of the tile, hidden row j % R)
+      for (int j = sw4; j < 2 * a.R; j += kWSelWarps) {
+        const int blk = j / a.R, m = j - blk * a.R;
+        const int b = tile * 2 + blk;
+        if (b >= a.nblk) continue;
+        const uint32_t* kc = keys + 64 * blk * PITCH + m;
+        uint32_t k0 = kc[lane * PITCH], k1 = kc[(lane + 32) * PITCH];
+        uint32_t key_lo = 0u, row_lo = 64u, key_hi = 0u, row_hi = 64u;  // slots lane, lane + 32
+        for (int r = 0; r < a.kcand; ++r) {
+          const bool first = k0 >= k1;
+          const uint32_t bk = first ? k0 : k1;
+          const uint32_t brow =
+              first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
+          const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+          const uint32_t rwin = __reduce_min_sync(0xffffffffu, bk == kmax ? brow : 64u);
+          if (kmax != 0u && lane == static_cast<int>(rwin & 31u)) {
+            if (rwin < 32u) k0 = 0u; else k1 = 0u;
+          }
+          if (lane == (r & 31)) {
+            if (r < 32) {
+              key_lo = kmax;
+              row_lo = kmax ? rwin : 64u;
+            } else {
+              key_hi = kmax;
+              row_hi = kmax ? rwin : 64u;
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(keys_free);
+        const int64_t obase = static_cast<int64_t>(a.m0 + m) * a.nblk * a.kcand +
+                              static_cast<int64_t>(b) * a.kcand;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int slot = lane + 32 * h;
+          const uint32_t kk = h ? key_hi : key_lo, rr = h ? row_hi : row_lo;
+          if (slot < a.kcand) {
+            a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
+            a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
+          }
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(keys_free);
     }
   }
 
@@ -590,8 +665,9 @@ static bool plan_wide(WideArgs& a, int ncol, int G, int max_smem, int* smem_byte
   const int ew_bytes = ncol * 4;
   const int bar_bytes = (2 * kWMaxNP + 2 * kWMaxNB + 2 * kWMaxNA + 4 + 3) * 8 + 16;
   const int fixed = sz_bytes + key_bytes + xs_bytes + ew_bytes + bar_bytes + 64 + 1024;
+  // an even number of B units: each of the two MMA issuers takes every other one
   int nbu = kWMaxNB, np = 0;
-  for (; nbu >= 2; --nbu) {
+  for (; nbu >= 2; nbu -= 2) {
     np = (max_smem - fixed - nbu * a.unit_bytes) / kWStageSmem;
     if (np >= 3) break;
   }
