@@ -465,6 +465,7 @@ def _end_to_end_checks(w, c, ov, oi, rr, rl, am, R):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("M,bits,G,kcand", [
+    (1, 2, 128, 8),    # the headline call (bench value: one hidden row, KCAND=8, R=16)
     (8, 4, 128, 1),    # the 4-bit comparison head (bench line int4_g128_m8_kcand1)
     (8, 2, 64, 8),     # the group-64 ablation (bench line int2_g64_m8_kcand8)
     (72, 2, 128, 8),   # the tensor-core pass, then the rerank (bench per_m 72)
