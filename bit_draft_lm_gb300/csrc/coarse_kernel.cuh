@@ -1,5 +1,5 @@
 // Coarse pass + block top-KCAND of the low-bit draft head (page "radiance_drafthead.py":
-// module docstring, _draft_head_int2 and _emit), for sm_103a.
+// module docstring, the int2 coarse kernel and the block candidate emission), for sm_103a.
 //
 // Work decomposition (GB300-first, not the page's one-program-per-block grid):
 //  * Persistent grid, one CTA per SM. A CTA walks 64-row candidate blocks b = blockIdx.x,

@@ -1,5 +1,6 @@
 // Coarse pass + block top-KCAND of the int2 draft head for many hidden rows at once (page
-// "radiance_drafthead.py": module docstring, _draft_head_int2 and _emit), on the
+// "radiance_drafthead.py": module docstring, the int2 coarse kernel and the block candidate
+// emission), on the
 // 5th-generation tensor cores of sm_103a: tcgen05.mma with the dequantised weights in tensor
 // memory (TMEM) and the hidden states in shared memory.
 //

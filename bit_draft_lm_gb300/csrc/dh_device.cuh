@@ -188,7 +188,7 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
   return r & 0xffu;
 }
 // e4m3 byte -> fp32 (the format's definition: bias 7, subnormals m * 2^-9; NaN not produced here).
-__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+__device__ __forceinline__ float e4m3_bits_to_f32(uint32_t b) {
   const uint32_t e = (b >> 3) & 15u, m = b & 7u;
   const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20))
                       : static_cast<float>(m) * 0.001953125f;  // m * 2^-9

@@ -1,8 +1,8 @@
-// Offline quantise + pack of the head weight (page "radiance_drafthead.py", _quantize_head_now):
+// Offline quantise + pack of the head weight (page "radiance_drafthead.py", the load-time quantiser):
 // asymmetric min/max codes per (vocab row, group of G along K), quarter-split int2 or half-split
 // int4 packing, premultiplied bf16 scale S = bf16(bias*sc) and zero term ZS = bf16(bias*sc + zp*sc).
 //
-// Input rows are bf16, or (FP8 checkpoints, the page's _head_matrix) e4m3 bytes with an fp32
+// Input rows are bf16, or (FP8 checkpoints, the page's FP8 head) e4m3 bytes with an fp32
 // per-row scale: w = e4m3(b) * scale[n], one fp32 multiply, as the page's `wg * wsc[i:j, None]`.
 //
 // One CTA per vocab row. Every floating-point step is a separately rounded IEEE fp32 operation
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         const uint32_t byte = ((b < 4 ? v.x : v.y) >> (8 * (b & 3))) & 0xffu;
-        w_row[8 * i + b] = __fmul_rn(e4m3_to_f32(byte), rs);
+        w_row[8 * i + b] = __fmul_rn(e4m3_bits_to_f32(byte), rs);
       }
     }
   } else {

@@ -1,5 +1,5 @@
 // Global top-RERANK over the block candidates, exact rerank and argmax (page
-// "radiance_drafthead.py": bm.topk(RERANK) + bi.gather in _apply_head_int2, _rerank_exact with
+// "radiance_drafthead.py": the head application's RERANK best candidates, the exact rerank with
 // bf16 rows, and the argmax its caller takes), for sm_103a.
 //
 // One CTA (1024 threads) per hidden row m:
@@ -111,12 +111,12 @@ __device__ __forceinline__ void w_pair(const uint4& w, int q, float& lo, float& 
   lo = __uint_as_float(v << 16);
   hi = __uint_as_float(v & 0xffff0000u);
 }
-// e4m3 bytes: the page's exact bit decode (e4m3_to_f32), no hardware conversion.
+// e4m3 bytes: the page's exact bit decode of its FP8 rerank, no hardware conversion.
 __device__ __forceinline__ void w_pair(const uint2& w, int q, float& lo, float& hi) {
   const uint32_t v = q < 2 ? w.x : w.y;
   const int sh = 16 * (q & 1);
-  lo = e4m3_to_f32((v >> sh) & 0xffu);
-  hi = e4m3_to_f32((v >> (sh + 8)) & 0xffu);
+  lo = e4m3_bits_to_f32((v >> sh) & 0xffu);
+  hi = e4m3_bits_to_f32((v >> (sh + 8)) & 0xffu);
 }
 template <bool FP8>
 __device__ __forceinline__ typename Row8<FP8>::Raw load_w8(const RerankArgs& a, int n, int k8);

@@ -1,5 +1,5 @@
-// Logits for a top-K caller (page "radiance_drafthead.py", _apply_head_int2 with
-// _radiance_topk_only): every entry of the row is -inf except the RERANK reranked ones, which
+// Logits for a top-K caller (page "radiance_drafthead.py", its top-K-only output of the head
+// application): every entry of the row is -inf except the RERANK reranked ones, which
 // carry their exact logit rounded to bf16, so a top-K request draws from the reranked pool only.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

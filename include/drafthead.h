@@ -1,8 +1,9 @@
 /*
  * drafthead.h -- C ABI of the GB300 (sm_103a) low-bit speculative-decoding draft head.
  *
- * The operation is the draft head of the page "radiance_drafthead.py" (module docstring;
- * _quantize_head_now, _draft_head_int2, _emit, _rerank_exact, _apply_head_int2):
+ * The operation is the draft head of the page "radiance_drafthead.py" (its module docstring;
+ * its load-time quantiser, int2 coarse kernel, block candidate emission, exact rerank and head
+ * application):
  *   logits = x[M, K] @ W^T for a vocabulary head W[N, K] (vocab rows, the lm_head layout),
  * computed coarsely from int2 (or int4) codes with an asymmetric per-(vocab row, group of G
  * along K) scale and zero point, after which each 64-row block keeps its KCAND largest coarse
@@ -56,8 +57,8 @@ enum {
 #define DH_DEV_BAD_ID 0x2u       /* the rerank met a candidate id >= N; that slot scored -inf */
 
 /*
- * Offline quantise + pack, int2 (_quantize_head_now with BITS = 2; docstring "Quarter-split
- * packing" and "Bit-pattern dequant, hoisted").
+ * Offline quantise + pack, int2 (page "radiance_drafthead.py", the load-time quantiser at
+ * two bits; module docstring on the quarter-split packing and the hoisted bit-pattern dequant).
  *   W       bf16 [N, K], the head weight, vocab rows.                              (16-B aligned)
  *   G       group size along K: 64 or 128.  Requires K % (4*G) == 0.
  *   packed  u8 [N, K/4] out: byte j of row n = q[j] | q[Q+j]<<2 | q[2Q+j]<<4 | q[3Q+j]<<6, Q=K/4.
@@ -78,8 +79,8 @@ int dh_quantize_pack_int4(const void* W, int64_t N, int64_t K, int G, uint8_t* p
                           void* ZS, dh_stream_t s);
 
 /*
- * The int2 quantiser on an FP8 head (_quantize_head_now on _head_matrix's e4m3 rows with their
- * per-row scale, the compressed-tensors per-channel FP8 lm_head): the values quantised are
+ * The int2 quantiser on an FP8 head (the load-time quantiser applied to the head's e4m3 rows
+ * with their per-row scale, the page's per-channel FP8 lm_head): the values quantised are
  * fp32(e4m3(W8[n, k])) * row_scale[n] (one fp32 multiply), then exactly as
  * dh_quantize_pack_int2.
  *   W8         e4m3 [N, K] row bytes (e4m3 decoded bit-exactly: no NaN handling).   (16-B aligned)
@@ -101,7 +102,8 @@ size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits);
 size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank);
 
 /*
- * Coarse pass + block top-KCAND (_draft_head_int2 followed by _emit).
+ * Coarse pass + block top-KCAND (the page's int2 coarse kernel and its block candidate
+ * emission).
  *   x         bf16 [M, K] hidden states, 1 <= M <= DH_MAX_TOKENS.                  (16-B aligned)
  *   packed,S,ZS  as written by dh_quantize_pack_int2 (bits=2) or _int4 (bits=4).  (16-B aligned)
  *   G         64 or 128; requires K % (8*G) == 0 and K <= 5120.
@@ -128,8 +130,9 @@ int dh_draft_head_coarse_topk(const void* x, int64_t M, int64_t K, const uint8_t
                               void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
- * Global top-RERANK over the block candidates, exact rerank, argmax (bm.topk + bi.gather,
- * _rerank_exact with bf16 rows, then the caller's argmax).
+ * Global top-RERANK over the block candidates, exact rerank, argmax (the page's head
+ * application after the coarse pass: the RERANK best candidates, their exact bf16 rescoring,
+ * then the caller's argmax).
  *   x         bf16 [M, K] (the same hidden states).                                (16-B aligned)
  *   W         bf16 [N, K] the exact head weight.                                   (16-B aligned)
  *   cand_val, cand_id  f32 / i32 [M, ncand] (any candidate list; ncand >= rerank).
@@ -150,7 +153,7 @@ int dh_draft_head_rerank_argmax(const void* x, int64_t M, int64_t K, const void*
                                 void* y_coarse, void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
- * The whole device-side call (the page's _apply_head_int2 from hidden states to the argmax):
+ * The whole device-side call (the page's head application from hidden states to the argmax):
  * dh_draft_head_coarse_topk followed by dh_draft_head_rerank_argmax on the same stream, with
  * the arguments and outputs of the two calls (ncand = ceil(N/64) * kcand; y_coarse, when given,
  * holds the coarse logits with the reranked entries scattered over them) and bit-identical
@@ -197,7 +200,8 @@ int dh_draft_head_rerank_argmax_noalloc(const void* x, int64_t M, int64_t K, con
                                         dh_stream_t s);
 
 /*
- * dh_draft_head_rerank_argmax against FP8 rows (_rerank_exact with FP8=True): the exact logit is
+ * dh_draft_head_rerank_argmax against FP8 rows (the page's exact rerank on its FP8 head): the
+ * exact logit is
  * sum_k x[m, k] * e4m3(W8[n, k]) * row_scale[n], the e4m3 bytes decoded bit-exactly; fp32
  * accumulation, the row scale applied to the sum. Every other argument and output as there.
  */
@@ -209,7 +213,7 @@ int dh_draft_head_rerank_argmax_fp8(const void* x, int64_t M, int64_t K, const u
                                     dh_stream_t s);
 
 /*
- * Logits for a top-K caller (_apply_head_int2 with _radiance_topk_only: y.fill_(-inf) then the
+ * Logits for a top-K caller (the page's top-K-only output: every logit -inf, then the
  * rerank's scatter): y [M, N] bf16 out = -inf everywhere except y[m, rr_id[m, j]] =
  * bf16(rr_logit[m, j]) (round to nearest even), so that a top-K request draws from exactly the
  * RERANK reranked entries. rr_id, rr_logit [M, rerank] as written by
@@ -247,7 +251,7 @@ int dh_argmax_merge_host(const int64_t* keys, int P, int64_t M, int32_t* argmax_
                          float* logit);
 
 /*
- * The whole call from and to host memory (_apply_head_int2 end to end): copies x_host (bf16
+ * The whole call from and to host memory (the page's head application end to end): copies x_host (bf16
  * [M, K]) into x_dev, runs dh_draft_head_argmax, copies
  * argmax [M], rr_id [M, rerank] and rr_logit [M, rerank] back into argmax_host, rr_id_host and
  * rr_logit_host, and synchronises (the one call besides dh_workspace_status that does).
@@ -271,7 +275,7 @@ int dh_draft_head_host(const void* x_host, int64_t M, int64_t K, void* x_dev,
                        void* workspace, size_t ws_bytes, dh_stream_t s);
 
 /*
- * A host-memory call prepared once (the page's _apply_head_int2 end to end, as
+ * A host-memory call prepared once (the page's head application end to end, as
  * dh_draft_head_host): dh_host_plan_create validates the arguments of
  * dh_draft_head_host (all but the stream) and captures the call into a CUDA graph that the plan
  * owns (on the current device); dh_host_plan_run replays it on s and synchronises s, so that a

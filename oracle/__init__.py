@@ -7,22 +7,22 @@ everything after it) through ctypes and shares no code with the CUDA library.
 Every function takes and returns numpy arrays; bf16 tensors are carried as their uint16 bit
 patterns. Functions and the passages they follow (page "radiance_drafthead.py"):
 
-* ``quantize_pack``   -- ``_quantize_head_now``: asymmetric min/max codes per (row, group),
+* ``quantize_pack``   -- the load-time quantiser: asymmetric min/max codes per (row, group),
                          quarter-split int2 / half-split int4 packing, S and ZS premultiplied.
-* ``unpack_codes``    -- the packing read back (docstring, "Quarter-split packing").
-* ``coarse``          -- ``_draft_head_int2``: ``sum_gi S*P_gi - ZS*XS_gi`` in fp64.
+* ``unpack_codes``    -- the packing read back (module docstring, on the quarter-split packing).
+* ``coarse``          -- the int2 coarse kernel: ``sum_gi S*P_gi - ZS*XS_gi`` in fp64.
 * ``coarse_dequant``  -- the same value as a dot with dequantised weights (fold self-check).
-* ``block_topk``      -- ``_emit``: top-KCAND per 64-row block.
-* ``global_topr``     -- ``bm.topk(RERANK)`` + ``bi.gather``.
-* ``rerank``          -- ``_rerank_exact``: exact logits of the selected rows.
+* ``block_topk``      -- the block candidate emission: top-KCAND per 64-row block.
+* ``global_topr``     -- the head application's RERANK best block candidates.
+* ``rerank``          -- the exact rerank: exact logits of the selected rows.
 * ``argmax``          -- the argmax the caller takes.
 * ``exact_logits``    -- brute force over every vocab row.
-* ``topk_only``       -- ``_radiance_topk_only``: ``y.fill_(-inf)`` then the rerank's scatter of
-                         ``ex.to(torch.bfloat16)`` at the reranked ids.
-* ``e4m3_decode``     -- ``_rerank_exact`` (FP8): the exact bit decode of an e4m3 byte.
-* ``quantize_pack_fp8`` -- ``_quantize_head_now`` on an FP8 head (``_head_matrix``): the e4m3
-                         values times the fp32 per-row scale, then the same quantiser.
-* ``rerank_fp8``      -- ``_rerank_exact`` with FP8 rows: sum_k x_k * e4m3(W8[n,k]) * scale[n].
+* ``topk_only``       -- the top-K-only output: every logit -inf, then the rerank's exact logits,
+                         rounded to bf16, at the reranked ids.
+* ``e4m3_decode``     -- the exact rerank on the FP8 head: the exact bit decode of an e4m3 byte.
+* ``quantize_pack_fp8`` -- the load-time quantiser on the FP8 head: the e4m3 values times the fp32
+                         per-row scale, then the same quantiser.
+* ``rerank_fp8``      -- the exact rerank with FP8 rows: sum_k x_k * e4m3(W8[n,k]) * scale[n].
 """
 from __future__ import annotations
 
@@ -217,7 +217,7 @@ def bf16_rne(v: np.ndarray) -> np.ndarray:
 
 def topk_only(rr_id: np.ndarray, rr_logit: np.ndarray, N: int) -> np.ndarray:
     """bf16 bits [M, N]: -inf (0xFF80) everywhere, then bf16(rr_logit[m, j]) at rr_id[m, j] --
-    the logits a top-K caller ranks (page: ``_radiance_topk_only``)."""
+    the logits a top-K caller ranks (page: the top-K-only output)."""
     M, R = rr_id.shape
     y = np.full((M, N), 0xFF80, dtype=np.uint16)
     for m in range(M):

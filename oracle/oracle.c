@@ -14,15 +14,15 @@
  *   orc_quantize_pack   asymmetric min/max quantiser, quarter-split (int2) or half-split (int4)
  *   orc_quantize_pack_f32  the same on fp32 rows (an FP8 head's scaled e4m3 values)
  *                       packing, premultiplied scale S and zero term ZS
- *                       (_quantize_head_now, "Asymmetric min/max at BITS, quarter-split packing").
+ *                       (the load-time quantiser; module docstring on the quarter-split packing).
  *   orc_coarse          c[m,n] = sum_gi ( S*P_gi - ZS*XS_gi ), P_gi = sum_k x_k (1 + v_k/beta),
- *                       XS_gi = sum_k x_k  (docstring "Bit-pattern dequant, hoisted" and the
- *                       kernel _draft_head_int2), beta = 4 (int2) or 16 (int4).
+ *                       XS_gi = sum_k x_k  (module docstring on the hoisted bit-pattern dequant,
+ *                       and the int2 coarse kernel), beta = 4 (int2) or 16 (int4).
  *   orc_coarse_dequant  the same value written as a dot with dequantised weights,
  *                       sum_k x_k ((S/beta) v_k - (ZS - S)), used as a self-check of the fold.
- *   orc_block_topk      per 64-row block, the KCAND largest coarse values (_emit).
- *   orc_global_topr     the R largest of a row's block candidates (bm.topk + bi.gather).
- *   orc_rerank          exact logit sum_k x_k W[n,k] for the selected rows (_rerank_exact).
+ *   orc_block_topk      per 64-row block, the KCAND largest coarse values (block candidate emission).
+ *   orc_global_topr     the R largest of a row's block candidates (head application).
+ *   orc_rerank          exact logit sum_k x_k W[n,k] for the selected rows (exact rerank).
  *   orc_argmax          the argmax the caller takes over the reranked logits.
  *   orc_exact_logits    brute force: the exact logit of every vocab row.
  * Ties: selections order by (value descending, row id ascending); the argmax takes the lowest id.
@@ -179,8 +179,8 @@ int orc_quantize_pack(const uint16_t* W, int64_t N, int64_t K, int G, int bits, 
 }
 
 /* The same quantiser on fp32 rows: an FP8 head's values e4m3(b) * row_scale (page
- * _quantize_head_now: `wg = w.data[i:j].to(torch.float32) * wsc[i:j, None]`, one fp32 multiply,
- * done by the caller). */
+ * "radiance_drafthead.py", the load-time quantiser on the FP8 head: the e4m3 values widened to
+ * fp32 and multiplied by the row's scale, one fp32 multiply, done by the caller). */
 int orc_quantize_pack_f32(const float* Wf, int64_t N, int64_t K, int G, int bits,
                           uint8_t* packed, uint16_t* S, uint16_t* ZS, int nthreads) {
   if (!Wf || !packed || !S || !ZS) return -1;

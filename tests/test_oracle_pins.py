@@ -2,8 +2,9 @@
 
 Each test ties one oracle step to something other than the oracle itself: hand-worked values
 (tests/golden), the page's own bit-pattern dequant, closed forms, brute force on tiny inputs,
-and the page's stated sizes. Page: "radiance_drafthead.py" (module docstring and
-_quantize_head_now / _draft_head_int2 / _emit / _rerank_exact / _apply_head_int2).
+and the page's stated sizes. Page: "radiance_drafthead.py" (module docstring, the load-time
+quantiser, the int2 coarse kernel, the block candidate emission, the exact rerank and the head
+application).
 """
 import os
 
@@ -234,7 +235,7 @@ def _brute_block_topk(c, kcand):
 @pytest.mark.parametrize("N,kcand", [(640, 8), (700, 8), (130, 1), (64, 64), (200, 3),
                                      (70, 8), (130, 4)])  # last block shorter than KCAND
 def test_block_topk_brute_force(N, kcand):
-    """Block top-KCAND by successive max-and-mask (_emit) == sorting each 64-row block by
+    """Block top-KCAND by successive max-and-mask (the block candidate emission) == sorting each 64-row block by
     (value desc, id asc); short last block padded with (-inf, -1); ties present."""
     rng = np.random.default_rng(N + kcand)
     c = np.round(rng.standard_normal((3, N)) * 4) / 4     # many exact ties
