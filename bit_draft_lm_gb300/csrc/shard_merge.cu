@@ -1,6 +1,6 @@
 // Vocabulary-sharded argmax merge (page "radiance_drafthead.py": module docstring, where the head
-// is x[M, 5120] @ W[5120, 124160] "per rank", and the launch-geometry notes that time one rank's
-// vocab shard). With the head's vocab rows split across ranks at 64-row block boundaries, each
+// is x[M, 5120] @ W[5120, 124160] on each rank, and the launch-geometry notes that time one
+// rank's vocab shard). With the head's vocab rows split across ranks at 64-row block boundaries, each
 // rank runs the whole path on its shard; its blocks' candidates are exactly the unsharded head's
 // blocks' candidates, so the only exchange is one per hidden row: the shard's best reranked
 // (logit, vocab id). Each shard turns it into one 64-bit key whose signed integer order is the
