@@ -16,24 +16,27 @@
 //    workspace: x * 2^(15 - E_m) / 4^p as f16 (E_m from max |x[m]|; plane p's codes are
 //    v * 4^p * 2^-24 as f16 subnormals, so every product is v x 2^(15 - E_m) 2^-24 exactly),
 //    grouped per (scale group J, plane p) into one contiguous unit; also the group sums XS.
-//  * Persistent grid, one CTA per SM, 128-row tiles (the MMA's M = TMEM lanes). Warp 0 streams
-//    the packed rows through a ring of 128 x 128-byte stages with 2-D tensor-map copies (TMA,
-//    128-byte swizzle); warp 2 streams the B units through a second ring with bulk copies.
-//  * 8 dequantising warps, two per TMEM lane quadrant (even and odd chunks of a group); the
-//    thread of TMEM lane r owns row r. A 16-byte chunk of its row (16 byte positions x 4 planes)
-//    gives, for one plane pair, 16 registers of f16 pairs with one AND each (the odd bytes come
-//    down by one shift per word), written to a TMEM A stage by one tcgen05.st: plane 2h + q's 16
-//    codes are the stage's columns 8q .. 8q + 7.
-//  * Two MMA-issuing threads (warps 1 and 3), one per plane of a pair, so that two independent
-//    accumulation chains keep the tensor pipe busy: for plane p of scale group J the group's
-//    chunks accumulate into one D slot (128 x N fp32); four D slots let one plane pair be folded
-//    while the next accumulates. So the page's per-group scale is applied to the accumulator,
-//    never to the weight tile: acc += S[n, g] * D_g. The zero-point part sum_g (S - ZS) XS_g
-//    (the page's S (XS + sum x v / 4) - ZS XS rearranged) is a per-row dot with the group sums.
-//  * 8 fold warps (two per TMEM lane quadrant, half of the columns each; thread = row) add
-//    S_g D_g and the zero-point part (S_g - ZS_g) XS_g of every slot into registers, then hand
-//    the tile's keys to 4 selection warps, which pick the top-KCAND of each 64-row block per
-//    hidden row (warp reductions on order-preserving keys, lowest row on ties).
+//  * Persistent grid, one CTA per SM, 128-row tiles (the MMA's M = TMEM lanes). One producer
+//    thread feeds two rings without blocking on either: the packed rows through 128 x 128-byte
+//    stages with 2-D tensor-map copies (TMA, 128-byte swizzle), and the B operand through
+//    half-units (half of a (scale group, plane)'s chunks) with bulk copies.
+//  * 8 dequantising warps, two per TMEM lane quadrant (even and odd chunks); the thread of TMEM
+//    lane r owns row r. A 16-byte chunk of its row (16 byte positions x 4 planes) becomes 32
+//    registers of f16 pairs with one AND each (the odd bytes come down by one shift per word),
+//    written to a 32-column TMEM A stage by one tcgen05.st: plane p's 16 codes are the stage's
+//    columns 8p .. 8p + 7.
+//  * Four MMA-issuing threads (warps 1 .. 4), one per plane: independent accumulation chains
+//    keep the tensor pipe busy (one thread issues an MMA only every ~100 ns). Plane p of scale
+//    group J accumulates the group's chunks into D slot p (128 x N fp32), so the page's
+//    per-group scale is applied to the accumulator, never to the weight tile:
+//    acc += S[n, g] * D_g. The zero-point part sum_g (S - ZS) XS_g (the page's
+//    S (XS + sum x v / 4) - ZS XS rearranged) is a per-row dot with the group sums. A stage is
+//    released when all four issuers' MMAs on it are done, a B half-unit when its issuer's are.
+//  * 8 fold warps (two per TMEM lane quadrant, half of the columns each; thread = row) read
+//    each D slot as soon as its group is complete, release it to its issuer, and add
+//    S_g D_g + (S_g - ZS_g) XS_g into registers; then they hand the tile's keys to 3 selection
+//    warps, which pick the top-KCAND of each 64-row block per hidden row (warp reductions on
+//    order-preserving keys, lowest row on ties).
 // Every wait is bounded (kWaitLimitNs); a wait that runs out marks the launch failed in the
 // status word, after which every wait returns at once and the kernel runs to its end.
 #include <cuda.h>
@@ -55,17 +58,18 @@ constexpr int kWStageBytes = 128;  // packed bytes of a row per ring stage (8 ch
 constexpr int kWStageSmem = kWRows * kWStageBytes;
 constexpr int kWDeqWarps = 8;   // dequantising: two per TMEM lane quadrant
 constexpr int kWFoldWarps = 8;  // fold: two per TMEM lane quadrant
-constexpr int kWSelWarps = 4;   // block top-KCAND selection
-// packed producer, MMA issuer A, B producer, MMA issuer B, then the dequantising, fold and
-// selection warps
-constexpr int kWDeq0 = 4;                         // first dequantising warp
-constexpr int kWFold0 = kWDeq0 + kWDeqWarps;      // first fold warp
-constexpr int kWSel0 = kWFold0 + kWFoldWarps;     // first selection warp
+constexpr int kWSelWarps = 3;   // block top-KCAND selection (off the critical path)
+constexpr int kWIssuers = 4;    // MMA-issuing threads: one per int2 plane
+// warp 0: the copy producer (one thread, both rings); warps 1 .. 4: the MMA issuers; then the
+// dequantising, fold and selection warps
+constexpr int kWDeq0 = 1 + kWIssuers;          // first dequantising warp
+constexpr int kWFold0 = kWDeq0 + kWDeqWarps;   // first fold warp
+constexpr int kWSel0 = kWFold0 + kWFoldWarps;  // first selection warp
 constexpr int kWWarps = kWSel0 + kWSelWarps;
 constexpr int kWThreads = kWWarps * 32;
 constexpr int kWMaxNP = 8;   // packed ring stages at most
-constexpr int kWMaxNB = 4;   // B ring units at most
-constexpr int kWMaxNA = 28;  // A stages at most (16 TMEM columns each)
+constexpr int kWNB = 8;      // B ring: two half-units per issuer
+constexpr int kWMaxNA = 14;  // A stages at most (32 TMEM columns each)
 constexpr int kWTmemCols = 512;
 constexpr int kWPrepThreads = 256;
 
@@ -170,31 +174,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
     coarse_wide_kernel(const __grid_constant__ CUtensorMap tmap, const WideArgs a) {
   constexpr int P = 4;           // int2 planes
   constexpr int CPJ = G / 16;    // chunks per scale group
-  constexpr int ACOLS = 16;      // TMEM columns of one A stage: one chunk, two planes
-  // Four D slots (two per plane pair, double-buffered by pair) at columns 0 .. 4 NCOL, then the
-  // A stages (chunk, plane pair), an even number: they are released in pairs (chunks 2q, 2q + 1)
+  constexpr int CPH = CPJ / 2;   // chunks per B half-unit
+  constexpr int ACOLS = 32;      // TMEM columns of one A stage: one chunk, four planes
+  // Four D slots (one per plane) at columns 0 .. 4 NCOL, then the A stages, an even number (the
+  // two dequantising parities own alternate stages)
   constexpr int NAS = ((kWTmemCols - 4 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
                                                                    : (kWTmemCols - 4 * NCOL) / ACOLS) &
                       ~1;
   constexpr int PITCH = NCOL + 1;  // words per row of the key buffer (odd: no bank conflicts)
   constexpr int HC = NCOL / 2;     // D columns of one fold warp
   static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 80, "MMA N");
-  static_assert(NAS >= CPJ + 2, "TMEM budget: a group's chunks plus one spare pair");
+  static_assert(NAS >= 2, "TMEM budget: at least one A stage per dequantising parity");
+  static_assert(CPH >= 1 && CPJ % 2 == 0, "B half-units");
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte alignment for the 128-byte swizzle of the packed ring
   unsigned char* sm = sm_raw + ((1024u - (smem_addr(sm_raw) & 1023u)) & 1023u);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int np = a.np, nbu = a.nbu;
+  const int np = a.np;
   uint64_t* pfull = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kWMaxNP] stage landed
   uint64_t* pempty = pfull + kWMaxNP;   // [kWMaxNP] stage read by the dequantising warps
-  uint64_t* bfull = pempty + kWMaxNP;   // [kWMaxNB] B unit landed
-  uint64_t* bempty = bfull + kWMaxNB;   // [kWMaxNB] B unit's D slot read (its MMAs are done)
-  uint64_t* afull = bempty + kWMaxNB;   // [kWMaxNA] A stage written
-  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA / 2] A stage pair's MMAs done
-  uint64_t* dfull = aempty + kWMaxNA;   // [2] D slot pair complete
-  uint64_t* dempty = dfull + 2;         // [2] D slot pair read by the fold warps
-  uint64_t* mma_done = dempty + 2;      // every MMA of the CTA complete
+  uint64_t* bfull = pempty + kWMaxNP;   // [kWNB] B half-unit landed
+  uint64_t* bempty = bfull + kWNB;      // [kWNB] B half-unit's MMAs done
+  uint64_t* afull = bempty + kWNB;      // [kWMaxNA] A stage written
+  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA] A stage's MMAs (all four issuers) done
+  uint64_t* dfull = aempty + kWMaxNA;   // [4] D slot p complete for the group
+  uint64_t* dempty = dfull + 4;         // [4] D slot p read by the fold warps
+  uint64_t* mma_done = dempty + 4;      // every MMA of the CTA complete
   uint64_t* keys_ready = mma_done + 1;  // a tile's keys written by the fold warps
   uint64_t* keys_free = mma_done + 2;   // ... and consumed by the selection warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 3);
@@ -204,26 +210,27 @@ __global__ void __launch_bounds__(kWThreads, 1)
       (a.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
       static_cast<int>(gridDim.x);
   const int total_stages = my_tiles * a.NS;
-  const int units_per_tile = a.NJ * P;
+  const int halves_per_tile = a.NJ * P * 2;
+  const int total_halves = my_tiles * halves_per_tile;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWMaxNP; ++i) {
       mbar_init(&pfull[i], 1u);
       mbar_init(&pempty[i], static_cast<uint32_t>(kWDeqWarps));
     }
-    for (int i = 0; i < kWMaxNB; ++i) {
+    for (int i = 0; i < kWNB; ++i) {
       mbar_init(&bfull[i], 1u);
-      mbar_init(&bempty[i], static_cast<uint32_t>(kWFoldWarps));
+      mbar_init(&bempty[i], 1u);  // its issuer's commit
     }
     for (int i = 0; i < kWMaxNA; ++i) {
-      mbar_init(&afull[i], 4u);  // the 4 quadrant warps of the stage's chunk parity
-      mbar_init(&aempty[i], 2u);  // one commit from each MMA issuer
+      mbar_init(&afull[i], 4u);   // the 4 quadrant warps of the stage's chunk parity
+      mbar_init(&aempty[i], static_cast<uint32_t>(kWIssuers));  // one commit per issuer
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&dfull[i], 2u);  // one commit from each MMA issuer
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&dfull[i], 1u);   // the slot's issuer
       mbar_init(&dempty[i], static_cast<uint32_t>(kWFoldWarps));
     }
-    mbar_init(mma_done, 2u);
+    mbar_init(mma_done, static_cast<uint32_t>(kWIssuers));
     mbar_init(keys_ready, static_cast<uint32_t>(kWFoldWarps));
     mbar_init(keys_free, static_cast<uint32_t>(kWSelWarps));
     *abort_flag = 0;
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_base = tmem + 4 * NCOL;  // column of A stage 0 (D slots at k NCOL, k < 4)
+  const uint32_t a_base = tmem + 4 * NCOL;  // column of A stage 0 (D slot p at p NCOL)
 
   // Bounded wait on one phase of an mbarrier: one test first (the common case costs one
   // instruction and no clock read), then suspended waits. Returns at once (false) once the launch
@@ -264,111 +271,119 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
   };
 
-  int issued = 0, issued_b = 0;  // copies issued by warp 0 / warp 2 (lane 0)
+  int issued = 0, issued_b = 0;  // copies issued into the packed and B rings (warp 0, lane 0)
   if (warp == 0) {
-    // ---- packed rows: ring stages in order. The first stages go to L2 while the preceding
-    // kernel may still run (it may have written the weights: only L2, which is coherent, is
-    // touched before griddepcontrol.wait); every copy into shared memory comes after the wait.
+    // ---- one producer thread for both rings, in consumption order, never blocked on one ring
+    // while the other has room. The first packed stages go to L2 while the preceding kernel may
+    // still run (it may have written the weights: only L2, which is coherent, is touched before
+    // griddepcontrol.wait); every copy into shared memory comes after the wait.
     if (lane == 0) {
       for (int s = 0; s < np && s < total_stages; ++s)
         tma_prefetch_l2_2d(&tmap, (s % a.NS) * kWStageBytes, tile_of(s / a.NS) * kWRows);
       grid_dependency_wait();
-      int slot = 0, lt = 0, s = 0;
-      uint32_t ph = 0u;
-      for (; issued < total_stages; ++issued) {
-        if (issued >= np) wait_bar(&pempty[slot], ph ^ 1u);
-        if (*abort_flag) break;
-        mbar_arrive_expect_tx(&pfull[slot], static_cast<uint32_t>(kWStageSmem));
-        tma_load_2d(sm + slot * kWStageSmem, &tmap, s * kWStageBytes, tile_of(lt) * kWRows,
-                    &pfull[slot]);
-        advance(slot, ph, np);
-        if (++s == a.NS) {
-          s = 0;
-          ++lt;
+      int pslot = 0, ps_in_tile = 0, plt = 0, bslot = 0, bunit = 0;
+      uint32_t pph = 0u, bph = 0u;
+      uint64_t t_idle = 0;
+      while ((issued < total_stages || issued_b < total_halves) && !*abort_flag) {
+        bool progress = false;
+        if (issued < total_stages &&
+            (issued < np || mbar_test_wait(&pempty[pslot], pph ^ 1u))) {
+          mbar_arrive_expect_tx(&pfull[pslot], static_cast<uint32_t>(kWStageSmem));
+          tma_load_2d(sm + pslot * kWStageSmem, &tmap, ps_in_tile * kWStageBytes,
+                      tile_of(plt) * kWRows, &pfull[pslot]);
+          advance(pslot, pph, np);
+          if (++ps_in_tile == a.NS) {
+            ps_in_tile = 0;
+            ++plt;
+          }
+          ++issued;
+          progress = true;
+        }
+        if (issued_b < total_halves &&
+            (issued_b < kWNB || mbar_test_wait(&bempty[bslot], bph ^ 1u))) {
+          // a group's half-units go out first halves first, plane by plane, so that the four
+          // issuers get theirs together: unit (J, h, p) of the order is (J, p, h) of the layout
+          const int uj = bunit >> 3, uh = (bunit >> 2) & 1, up = bunit & 3;
+          mbar_arrive_expect_tx(&bfull[bslot], static_cast<uint32_t>(a.unit_bytes));
+          bulk_g2s(sm + a.off_bring + bslot * a.unit_bytes,
+                   a.bbuf + static_cast<int64_t>((uj * 4 + up) * 2 + uh) * a.unit_bytes,
+                   static_cast<uint32_t>(a.unit_bytes), &bfull[bslot]);
+          advance(bslot, bph, kWNB);
+          if (++bunit == halves_per_tile) bunit = 0;
+          ++issued_b;
+          progress = true;
+        }
+        if (progress) {
+          t_idle = 0;
+        } else {
+          const uint64_t now = global_timer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_status(a.status, DH_DEV_WAIT_TIMEOUT);
+          }
+          __nanosleep(64);
         }
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // ---- B units (the prep kernel's output): one per (tile, group, plane), in MMA order --------
-    if (lane == 0) {
-      grid_dependency_wait();
-      const int total_units = my_tiles * units_per_tile;
-      int slot = 0, unit = 0;
-      uint32_t ph = 0u;
-      for (; issued_b < total_units; ++issued_b) {
-        if (issued_b >= nbu) wait_bar(&bempty[slot], ph ^ 1u);
-        if (*abort_flag) break;
-        mbar_arrive_expect_tx(&bfull[slot], static_cast<uint32_t>(a.unit_bytes));
-        bulk_g2s(sm + a.off_bring + slot * a.unit_bytes,
-                 a.bbuf + static_cast<int64_t>(unit) * a.unit_bytes,
-                 static_cast<uint32_t>(a.unit_bytes), &bfull[slot]);
-        advance(slot, ph, nbu);
-        if (++unit == units_per_tile) unit = 0;
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1 || warp == 3) {
-    // ---- MMA issue, two threads (one tcgen05.mma stream each, so that the tensor pipe overlaps
-    // them): issuer pl takes plane 2h + pl of every (group J, plane pair h), the group's chunks
-    // into D slot 2k + pl (k the pair's parity), A from the pair's stages, which both issuers
-    // release two by two. Descriptors and ring positions move by additions only.
-    const int pl = warp == 3 ? 1 : 0;
+  } else if (warp <= kWIssuers) {
+    // ---- MMA issue: issuer p = warp - 1 takes plane p of every scale group: the group's chunks
+    // into D slot p, A from the chunk's stage (columns 8p .. 8p + 7), B from its two half-units
+    // (ring slots p and 4 + p, one phase per group). Descriptors and ring positions move by
+    // additions only.
+    const int p = warp - 1;
     if (lane == 0) {
       const uint32_t idesc = tc_idesc_f16(kWRows, NCOL);
       const uint64_t bdesc0 = tc_sdesc(smem_addr(sm + a.off_bring), NCOL * 16, 128u);
-      int bslot = pl;  // this issuer's B units: every other unit of the ring (nbu is even)
+      const uint32_t d = tmem + p * NCOL, a_col = a_base + 8 * p;
       uint32_t bph = 0u;
       int as = 0;
       uint32_t aph = 0u;
-      int pr = 0;  // pairs issued; D slot 2 (pr & 1) + pl
+      int grp = 0;  // groups issued
       for (int lt = 0; lt < my_tiles; ++lt) {
-        for (int J = 0; J < a.NJ; ++J) {
-          for (int h = 0; h < 2; ++h, ++pr) {
-            const int k = pr & 1;
+        for (int J = 0; J < a.NJ; ++J, ++grp) {
+          if (grp > 0) wait_bar(&dempty[p], static_cast<uint32_t>(grp - 1) & 1u);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int bslot = 4 * hh + p;
             wait_bar(&bfull[bslot], bph);
-            if (pr >= 2) wait_bar(&dempty[k], static_cast<uint32_t>((pr >> 1) - 1) & 1u);
             tc_fence_after();
             const uint64_t bd = bdesc0 + static_cast<uint64_t>((bslot * a.unit_bytes) >> 4);
-            const uint32_t d = tmem + (2 * k + pl) * NCOL;
 #pragma unroll 2
-            for (int cj = 0; cj < CPJ; ++cj) {
+            for (int cj = 0; cj < CPH; ++cj) {
               wait_bar(&afull[as], aph);
               tc_fence_after();
-              tc_mma_f16_ts(d, a_base + as * ACOLS + 8 * pl,
+              tc_mma_f16_ts(d, a_col + as * ACOLS,
                             bd + static_cast<uint64_t>((cj * 2 * NCOL * 16) >> 4), idesc,
-                            cj != 0);
-              if (cj & 1) tc_commit(&aempty[as >> 1]);
+                            (hh | cj) != 0);
+              tc_commit(&aempty[as]);
               advance(as, aph, NAS);
             }
-            // one commit per pair and issuer: the fold warps that read the two slots release the
-            // B units
-            tc_commit(&dfull[k]);
-            bslot += 2;
-            if (bslot >= nbu) {
-              bslot -= nbu;
-              bph ^= 1u;
-            }
+            tc_commit(&bempty[bslot]);  // the half-unit's MMAs done: the producer may refill it
           }
+          tc_commit(&dfull[p]);
+          bph ^= 1u;
         }
       }
       tc_commit(mma_done);
       mbar_wait_bounded(mma_done, 0u);  // also after an abort: no MMA may outlive the TMEM
     }
     __syncwarp();
-  } else if (warp >= kWDeq0 && warp < kWFold0) {
+  } else if (warp < kWFold0) {
     // ---- dequantisation: eight warps, two per TMEM lane quadrant (one for the even chunks of a
-    // group, one for the odd), one thread per row. A stage holds one chunk's two planes of a pair
-    // (16 columns): planes 2h, 2h + 1 of 16 byte positions as f16 pairs (one AND each).
+    // group, one for the odd), one thread per row. A stage holds one chunk's four planes
+    // (32 columns) of 16 byte positions as f16 pairs (one AND each).
     const int sub = (warp - kWDeq0) >> 2;  // chunk parity of this warp
     const int row = (warp & 3) * 32 + lane;
     const uint32_t my_a = a_base + tmem_lane_base(warp);
     const int sw = row & 7;
     int ps = 0;  // packed ring slot of the current stage
     uint32_t pph = 0u;
-    int as0 = 0;  // A ring slot of the current pair's chunk 0
-    uint32_t aph0 = 0u;
-    int a_issued0 = 0;  // A stages the whole pass has begun before the current pair
+    int as = sub;  // A ring slot of this warp's next chunk (the parities alternate: NAS is even)
+    uint32_t aph = 0u;
+    int done0 = 0;  // chunks of the pass before the current group
     for (int lt = 0; lt < my_tiles; ++lt) {
       for (int J = 0; J < a.NJ; ++J) {
         const int c0 = J * CPJ;  // the group's first chunk within the tile
@@ -377,47 +392,38 @@ __global__ void __launch_bounds__(kWThreads, 1)
           __syncwarp();
         }
         const unsigned char* prow = sm + ps * kWStageSmem + row * kWStageBytes;
-        for (int h = 0; h < 2; ++h) {
-          for (int cj = sub; cj < CPJ; cj += 2) {
-            int as = as0 + cj;
-            uint32_t aph = aph0;
-            if (as >= NAS) {
-              as -= NAS;
-              aph ^= 1u;
-            }
-            if (a_issued0 + cj >= NAS) {  // the stage's previous MMAs are done
-              wait_bar(&aempty[as >> 1], aph ^ 1u);
-              __syncwarp();
-            }
-            tc_fence_after();
-            const int c = c0 + cj;
-            const uint4 w4 =
-                *reinterpret_cast<const uint4*>(prow + ((((c & 7) ^ sw)) << 4));
-            const uint32_t t[4] = {w4.x, w4.y, w4.z, w4.w};
-            uint32_t r[16];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const uint32_t te = t[w], to = t[w] >> 8;
-#pragma unroll
-              for (int pp = 0; pp < 2; ++pp) {
-                const uint32_t mk = 0x00030003u << (2 * (2 * h + pp));
-                r[8 * pp + 2 * w] = te & mk;
-                r[8 * pp + 2 * w + 1] = to & mk;
-              }
-            }
-            tmem_st_x16(my_a + as * ACOLS, r);
-            tmem_wait_st();
-            tc_fence_before();
+        for (int cj = sub; cj < CPJ; cj += 2) {
+          if (done0 + cj >= NAS) {  // the stage's previous MMAs are done
+            wait_bar(&aempty[as], aph ^ 1u);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[as]);
           }
-          as0 += CPJ;
-          a_issued0 += CPJ;
-          if (as0 >= NAS) {
-            as0 -= NAS;
-            aph0 ^= 1u;
+          tc_fence_after();
+          const int c = c0 + cj;
+          const uint4 w4 = *reinterpret_cast<const uint4*>(prow + ((((c & 7) ^ sw)) << 4));
+          const uint32_t t[4] = {w4.x, w4.y, w4.z, w4.w};
+          uint32_t r[32];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t te = t[w], to = t[w] >> 8;
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+              const uint32_t mk = 0x00030003u << (2 * q);
+              r[8 * q + 2 * w] = te & mk;
+              r[8 * q + 2 * w + 1] = to & mk;
+            }
+          }
+          tmem_st_x32(my_a + as * ACOLS, r);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[as]);
+          as += 2;
+          if (as >= NAS) {
+            as -= NAS;
+            aph ^= 1u;
           }
         }
+        done0 += CPJ;
         if (((c0 + CPJ) & 7) == 0) {  // the packed stage's last group: release it
           __syncwarp();
           if (lane == 0) mbar_arrive(&pempty[ps]);
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
       }
     }
-  } else if (warp >= kWFold0 && warp < kWSel0) {
+  } else if (warp < kWSel0) {
     // ---- fold: two warps per TMEM lane quadrant, each NCOL/2 columns of its 32 rows ------------
     const int fw = warp - kWFold0;  // 0..7
     const int half = fw >> 2;
@@ -468,8 +474,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       xsd[gi * NCOL + m] = a.xs[i] * w_pow2(-(a.ew[m] + 7));
     }
     named_bar_sync(2, kWFoldWarps * 32);
-    int gslot = 0, bslot = 0;
-    uint32_t bph = 0u;
+    int grp = 0;
     constexpr int kBatch = 24;  // D columns loaded per wait (three 8-column loads)
     for (int lt = 0; lt < my_tiles; ++lt) {
       const int n = tile_of(lt) * kWRows + row;
@@ -479,27 +484,24 @@ __global__ void __launch_bounds__(kWThreads, 1)
       float acc[HC];
 #pragma unroll
       for (int m = 0; m < HC; ++m) acc[m] = 0.0f;
-      // the tile's D slots, in the order the MMAs complete them: (group J, plane p); each adds
-      // S_g D_g and the zero-point part (S_g - ZS_g) XS_g
-      for (int J = 0; J < a.NJ; ++J) {
+      // the group's D slots as their issuers complete them; each adds S_g D_g and the
+      // zero-point part (S_g - ZS_g) XS_g, and goes back to its issuer once read
+      for (int J = 0; J < a.NJ; ++J, ++grp) {
         for (int p = 0; p < P; ++p) {
-          // pair pr = gslot of plane p: planes 2h, 2h + 1 complete together in slots 2k, 2k + 1
-          const int k = gslot & 1, gi = p * a.NJ + J, dbuf = 2 * k + (p & 1);
-          if ((p & 1) == 0) {
-            wait_bar(&dfull[k], static_cast<uint32_t>(gslot >> 1) & 1u);
-            __syncwarp();
-            tc_fence_after();
-          }
+          const int gi = p * a.NJ + J;
+          wait_bar(&dfull[p], static_cast<uint32_t>(grp) & 1u);
+          __syncwarp();
+          tc_fence_after();
           const float sg = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(s_row + 2 * gi));
           const float zg = sg - bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(z_row + 2 * gi));
           const float4* xg4 = reinterpret_cast<const float4*>(xsd + gi * NCOL + col0);
 #pragma unroll
           for (int q0 = 0; q0 < HC; q0 += kBatch) {
             constexpr int kB = kBatch;
-            uint32_t d[kB];
+            uint32_t dv[kB];
 #pragma unroll
             for (int q = 0; q < kB; q += 8)
-              if (q0 + q < HC) tmem_ld<8>(my_d + dbuf * NCOL + q0 + q, d + q);
+              if (q0 + q < HC) tmem_ld<8>(my_d + p * NCOL + q0 + q, dv + q);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < kB; q += 4) {
@@ -509,19 +511,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                   acc[q0 + q + i] =
-                      fmaf(sg, __uint_as_float(d[q + i]), fmaf(zg, xv[i], acc[q0 + q + i]));
+                      fmaf(sg, __uint_as_float(dv[q + i]), fmaf(zg, xv[i], acc[q0 + q + i]));
               }
             }
           }
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bempty[bslot]);  // the slot's MMAs, so its B unit, are done
-          advance(bslot, bph, nbu);
-          if (p & 1) {  // both slots of the pair are read
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dempty[k]);
-            ++gslot;
-          }
+          if (lane == 0) mbar_arrive(&dempty[p]);
         }
       }
       named_bar_sync(2, kWFoldWarps * 32);  // both halves are done with the tile's S and ZS rows
@@ -553,43 +549,68 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const int tile = tile_of(lt);
       wait_bar(keys_ready, static_cast<uint32_t>(lt) & 1u);
       __syncwarp();
-      // job j = (64-row block j / R of the tile, hidden row j % R)
-      for (int j = sw4; j < 2 * a.R; j += kWSelWarps) {
-        const int blk = j / a.R, m = j - blk * a.R;
-        const int b = tile * 2 + blk;
-        if (b >= a.nblk) continue;
-        const uint32_t* kc = keys + 64 * blk * PITCH + m;
-        uint32_t k0 = kc[lane * PITCH], k1 = kc[(lane + 32) * PITCH];
-        uint32_t key_lo = 0u, row_lo = 64u, key_hi = 0u, row_hi = 64u;  // slots lane, lane + 32
+      // job j = (64-row block j / R of the tile, hidden row j % R); a warp runs JB jobs at once
+      // so that their warp reductions overlap (each round of one job is a chain of two)
+      constexpr int JB = 4;
+      for (int j0 = sw4 * JB; j0 < 2 * a.R; j0 += kWSelWarps * JB) {
+        uint32_t k0[JB], k1[JB], key_lo[JB], row_lo[JB], key_hi[JB], row_hi[JB];
+        int bb[JB], mm[JB];
+#pragma unroll
+        for (int u = 0; u < JB; ++u) {
+          const int jj = j0 + u;
+          const int blk = jj / a.R;
+          mm[u] = jj - blk * a.R;
+          bb[u] = tile * 2 + blk;
+          const bool live = jj < 2 * a.R && bb[u] < a.nblk;
+          const uint32_t* kc = keys + 64 * blk * PITCH + mm[u];
+          k0[u] = live ? kc[lane * PITCH] : 0u;
+          k1[u] = live ? kc[(lane + 32) * PITCH] : 0u;
+          key_lo[u] = key_hi[u] = 0u;  // slots lane, lane + 32
+          row_lo[u] = row_hi[u] = 64u;
+          if (!live) bb[u] = -1;
+        }
         for (int r = 0; r < a.kcand; ++r) {
-          const bool first = k0 >= k1;
-          const uint32_t bk = first ? k0 : k1;
-          const uint32_t brow =
-              first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
-          const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-          const uint32_t rwin = __reduce_min_sync(0xffffffffu, bk == kmax ? brow : 64u);
-          if (kmax != 0u && lane == static_cast<int>(rwin & 31u)) {
-            if (rwin < 32u) k0 = 0u; else k1 = 0u;
+          uint32_t bk[JB], brow[JB], kmax[JB], rwin[JB];
+#pragma unroll
+          for (int u = 0; u < JB; ++u) {
+            const bool first = k0[u] >= k1[u];
+            bk[u] = first ? k0[u] : k1[u];
+            brow[u] = first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
+            kmax[u] = __reduce_max_sync(0xffffffffu, bk[u]);
           }
-          if (lane == (r & 31)) {
-            if (r < 32) {
-              key_lo = kmax;
-              row_lo = kmax ? rwin : 64u;
-            } else {
-              key_hi = kmax;
-              row_hi = kmax ? rwin : 64u;
+#pragma unroll
+          for (int u = 0; u < JB; ++u)
+            rwin[u] = __reduce_min_sync(0xffffffffu, bk[u] == kmax[u] ? brow[u] : 64u);
+#pragma unroll
+          for (int u = 0; u < JB; ++u) {
+            if (kmax[u] != 0u && lane == static_cast<int>(rwin[u] & 31u)) {
+              if (rwin[u] < 32u) k0[u] = 0u; else k1[u] = 0u;
+            }
+            if (lane == (r & 31)) {
+              if (r < 32) {
+                key_lo[u] = kmax[u];
+                row_lo[u] = kmax[u] ? rwin[u] : 64u;
+              } else {
+                key_hi[u] = kmax[u];
+                row_hi[u] = kmax[u] ? rwin[u] : 64u;
+              }
             }
           }
         }
-        const int64_t obase = static_cast<int64_t>(a.m0 + m) * a.nblk * a.kcand +
-                              static_cast<int64_t>(b) * a.kcand;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int slot = lane + 32 * h;
-          const uint32_t kk = h ? key_hi : key_lo, rr = h ? row_hi : row_lo;
-          if (slot < a.kcand) {
-            a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
-            a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
+        for (int u = 0; u < JB; ++u) {
+          if (bb[u] < 0) continue;
+          const int b = bb[u];
+          const int64_t obase = static_cast<int64_t>(a.m0 + mm[u]) * a.nblk * a.kcand +
+                                static_cast<int64_t>(b) * a.kcand;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int slot = lane + 32 * h;
+            const uint32_t kk = h ? key_hi[u] : key_lo[u], rr = h ? row_hi[u] : row_lo[u];
+            if (slot < a.kcand) {
+              a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
+              a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
+            }
           }
         }
       }
@@ -599,15 +620,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 0 || warp == 2) {
+  if (warp == 0) {
     // after an abort, copies may still be in flight: they land before the CTA's shared memory
     // goes away
     if (lane == 0 && *abort_flag) {
-      const int n_iss = warp == 0 ? issued : issued_b, depth = warp == 0 ? np : nbu;
-      uint64_t* bars = warp == 0 ? pfull : bfull;
-      for (int s = 0; s < depth && s < n_iss; ++s) {
-        const int last = n_iss - 1 - ((n_iss - 1 - s) % depth);
-        mbar_wait_bounded(&bars[s], static_cast<uint32_t>(last / depth) & 1u);
+      for (int ring = 0; ring < 2; ++ring) {
+        const int n_iss = ring == 0 ? issued : issued_b, depth = ring == 0 ? np : kWNB;
+        uint64_t* bars = ring == 0 ? pfull : bfull;
+        for (int s = 0; s < depth && s < n_iss; ++s) {
+          const int last = n_iss - 1 - ((n_iss - 1 - s) % depth);
+          mbar_wait_bounded(&bars[s], static_cast<uint32_t>(last / depth) & 1u);
+        }
       }
     }
     __syncwarp();
@@ -658,22 +681,19 @@ bool coarse_wide_supports(const CoarseCall& cc) {
 // Shared-memory plan of a pass; false if the rings do not fit.
 static bool plan_wide(WideArgs& a, int ncol, int G, int max_smem, int* smem_bytes) {
   const int cpj = G / 16;
-  a.unit_bytes = cpj * 2 * ncol * 16;
+  a.unit_bytes = (cpj / 2) * 2 * ncol * 16;  // a B half-unit
   a.szp = a.KG * 2;
   const int sz_bytes = 2 * kWRows * a.szp;
   const int key_bytes = kWRows * (ncol + 1) * 4;
   const int xs_bytes = ncol * a.KG * 4;
   const int ew_bytes = ncol * 4;
-  const int bar_bytes = (2 * kWMaxNP + 2 * kWMaxNB + 2 * kWMaxNA + 4 + 3) * 8 + 16;
+  const int bar_bytes = (2 * kWMaxNP + 2 * kWNB + 2 * kWMaxNA + 8 + 3) * 8 + 16;
   const int fixed = sz_bytes + key_bytes + xs_bytes + ew_bytes + bar_bytes + 64 + 1024;
-  // an even number of B units: each of the two MMA issuers takes every other one
-  int nbu = kWMaxNB, np = 0;
-  for (; nbu >= 2; nbu -= 2) {
-    np = (max_smem - fixed - nbu * a.unit_bytes) / kWStageSmem;
-    if (np >= 3) break;
-  }
+  // the B ring holds two half-units per issuer
+  const int nbu = kWNB;
+  int np = (max_smem - fixed - nbu * a.unit_bytes) / kWStageSmem;
   if (np > kWMaxNP) np = kWMaxNP;
-  if (nbu < 2 || np < 3) return false;
+  if (np < 3) return false;
   a.np = np;
   a.nbu = nbu;
   a.off_bring = np * kWStageSmem;
