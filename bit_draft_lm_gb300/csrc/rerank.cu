@@ -394,36 +394,35 @@ __global__ void __launch_bounds__(kRerankThreads, 1) rerank_argmax_kernel(const 
 
 
 // ---- Cluster path (R <= 32, ncand <= 16384): one cluster of kRC CTAs per hidden row. The CTAs
-// split the row's candidate slots, coordinate through distributed shared memory (no global
-// round trips between phases) and each computes R / kRC of the exact dots:
-//  1. every CTA loads its slots (keys and ids in registers) and its copy of x; its warp maxima
-//     go to CTA 0;
-//  2. CTA 0 takes T = the R-th largest of the kRC * 8 warp maxima (a lower bound of the R-th
-//     largest candidate, as in the single-CTA kernel) and sends it to every CTA;
-//  3. every CTA appends its candidates with key >= T to CTA 0's survivor list;
-//  4. CTA 0 selects the R first survivors in the selection order (or, if the list overflowed,
-//     runs the exact R-round selection over the whole row) and sends the ids to every CTA;
-//  5. CTA r computes the dots of slots r, r + kRC, ...; CTA 0 takes the argmax.
+// split the row's candidate slots and coordinate through distributed shared memory (no global
+// round trips between phases, three cluster barriers); each computes R / kRC of the exact dots:
+//  1. every CTA loads its slots (keys and ids in registers) and its copy of x, and sends its warp
+//     maxima to every CTA of the cluster;
+//  2. every CTA takes T = the R-th largest of the kRC * 8 warp maxima (a lower bound of the R-th
+//     largest candidate, as in the single-CTA kernel) and writes its candidates with key >= T
+//     into its own region of every CTA's survivor list;
+//  3. every CTA selects the R first survivors in the selection order (the same ids everywhere;
+//     or, if a region overflowed, runs the exact R-round selection over the whole row);
+//  4. CTA r computes the dots of slots r, r + kRC, ...; CTA 0 takes the argmax.
 constexpr int kRC = 8;
 constexpr int kRCThreads = 256;
 constexpr int kRCWarps = kRCThreads / 32;
 constexpr int kRCMaxLPT = 8;
-constexpr int kRCSurvCap = 256;
+constexpr int kRCRegion = 64;  // survivors one CTA may place in each CTA's list
 constexpr int kRCMaxR = 32;
 constexpr int kRCMaxCand = kRC * kRCThreads * kRCMaxLPT;  // 16384
 
 struct RCShared {
-  uint32_t allmax[kRC * kRCWarps];  // CTA 0: warp maxima of the cluster
-  uint32_t T;                       // threshold (every CTA)
-  int surv_n;                       // CTA 0: survivors appended
-  int base;                         // this CTA's first survivor position
+  uint32_t allmax[kRC * kRCWarps];  // the warp maxima of the cluster
+  uint32_t T;                       // threshold
   int wcnt[kRCWarps];
-  Sel surv[kRCSurvCap];          // CTA 0: survivors
-  Sel wbest[kRCWarps + 1];       // CTA 0 slow path
-  int32_t rr[kRCMaxR];           // selected ids (every CTA)
-  float part[4][kRCWarps];       // dot partials per warp, up to 4 slots per CTA
-  float logit[kRCMaxR];          // CTA 0: reranked logits
-  uint32_t retired[kRCMaxCand / 32];  // CTA 0 slow path: retired slots
+  int rcnt[kRC];                    // survivors each CTA placed here (may exceed kRCRegion)
+  Sel surv[kRC * kRCRegion];        // survivors, region r from CTA r
+  Sel wbest[kRCWarps + 1];          // slow path
+  int32_t rr[kRCMaxR];              // selected ids
+  float part[4][kRCWarps];          // dot partials per warp, up to 4 slots per CTA
+  float logit[kRCMaxR];             // CTA 0: reranked logits
+  uint32_t retired[kRCMaxCand / 32];  // slow path: retired slots
 };
 
 template <typename T>
@@ -436,8 +435,6 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     rerank_cluster_kernel(const RerankArgs a) {
   cg::cluster_group cl = cg::this_cluster();
   __shared__ RCShared sh;
-  extern __shared__ __align__(16) unsigned char rc_dyn[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(rc_dyn);  // [K]
   const int rank = static_cast<int>(cl.block_rank());
   const int m = blockIdx.x / kRC;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -450,12 +447,12 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
   if (tid == 0) grid_launch_dependents();
 
   // 1. once the preceding kernel has completed and its writes are visible (programmatic
-  // dependent launch; a no-op otherwise): x for the dots (it may be that kernel's output),
-  // then the keys and ids of this CTA's slots. Before the wait, x is only fetched into L2.
+  // dependent launch; a no-op otherwise): the keys and ids of this CTA's slots. x, which the dots
+  // read straight from global memory (it may be that kernel's output), is only fetched into L2
+  // before the wait.
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
   if (tid < a.K / 64) prefetch_l2(xr + 8 * tid);
   grid_dependency_wait();
-  for (int i = tid; i < a.K / 8; i += kRCThreads) reinterpret_cast<uint4*>(xs)[i] = xr[i];
   uint32_t key[LPT], uid[LPT];
 #pragma unroll
   for (int j = 0; j < LPT; ++j) {
@@ -467,12 +464,13 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
 #pragma unroll
   for (int j = 0; j < LPT; ++j) tmax = max(tmax, key[j]);
   tmax = __reduce_max_sync(0xffffffffu, tmax);
-  if (rank == 0 && tid == 0) sh.surv_n = 0;
-  if (lane == 0) cta0(cl, sh.allmax)[rank * kRCWarps + warp] = tmax;
+  // every CTA receives every warp maximum (lane r writes CTA r's copy)
+  if (lane < kRC) cl.map_shared_rank(sh.allmax, lane)[rank * kRCWarps + warp] = tmax;
   cl.sync();
 
-  // 2. T: the R-th largest warp maximum (rank of each value by counting, ties by position)
-  if (rank == 0 && warp == 0) {
+  // 2. T: the R-th largest warp maximum (rank of each value by counting, ties by position), the
+  // same in every CTA; then this CTA's candidates with key >= T into its region of every CTA
+  if (warp == 0) {
     const uint32_t v0 = sh.allmax[lane], v1 = sh.allmax[32 + lane];
     int r0 = 0, r1 = 0;
     for (int src = 0; src < 32; ++src) {
@@ -483,11 +481,9 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     }
     const uint32_t T = __reduce_max_sync(
         0xffffffffu, max(r0 == a.R - 1 ? v0 : 0u, r1 == a.R - 1 ? v1 : 0u));
-    if (lane < kRC) cl.map_shared_rank(&sh.T, lane)[0] = T;
+    if (lane == 0) sh.T = T;
   }
-  cl.sync();
-
-  // 3. survivors (key >= T) into CTA 0's list
+  __syncthreads();
   {
     const uint32_t T = sh.T;
     int cnt = 0;
@@ -501,51 +497,66 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     }
     if (lane == 31) sh.wcnt[warp] = incl;
     __syncthreads();
-    if (tid == 0) {
-      int tot = 0;
-      for (int w = 0; w < kRCWarps; ++w) tot += sh.wcnt[w];
-      sh.base = tot ? atomicAdd(cta0(cl, &sh.surv_n), tot) : 0;
+    int pos = incl - cnt, tot = 0;
+    for (int w = 0; w < kRCWarps; ++w) {
+      if (w < warp) pos += sh.wcnt[w];
+      tot += sh.wcnt[w];
     }
-    __syncthreads();
-    int pos = sh.base + incl - cnt;
-    for (int w = 0; w < warp; ++w) pos += sh.wcnt[w];
-    Sel* surv0 = cta0(cl, sh.surv);
 #pragma unroll
     for (int j = 0; j < LPT; ++j)
       if (key[j] != 0u && key[j] >= T) {
-        if (pos < kRCSurvCap)
-          surv0[pos] = Sel{key[j], uid[j], static_cast<uint32_t>(s0 + tid + j * kRCThreads)};
+        if (pos < kRCRegion) {
+          const Sel v{key[j], uid[j], static_cast<uint32_t>(s0 + tid + j * kRCThreads)};
+          for (int c = 0; c < kRC; ++c) cl.map_shared_rank(sh.surv, c)[rank * kRCRegion + pos] = v;
+        }
         ++pos;
       }
+    if (tid < kRC) cl.map_shared_rank(sh.rcnt, tid)[rank] = tot;
   }
   cl.sync();
 
-  // 4. CTA 0 selects the R first in selection order and sends the ids to every CTA
-  if (rank == 0) {
-    const int total = sh.surv_n;
-    if (total <= kRCSurvCap) {
+  // 3. every CTA: the R first survivors in selection order (identical lists, identical ids)
+  {
+    int total = 0;
+    bool overflow = false;
+    for (int c = 0; c < kRC; ++c) {
+      total += sh.rcnt[c];
+      overflow = overflow || sh.rcnt[c] > kRCRegion;
+    }
+    if (!overflow) {
       if (warp == 0) {
         if (total <= 32) {
-          Sel v = lane < total ? sh.surv[lane] : Sel{0u, 0xffffffffu, 0xffffffffu};
+          Sel v{0u, 0xffffffffu, 0xffffffffu};
+          if (lane < total) {
+            int c = 0, l = lane;
+            while (l >= sh.rcnt[c]) {
+              l -= sh.rcnt[c];
+              ++c;
+            }
+            v = sh.surv[c * kRCRegion + l];
+          }
           v = warp_sort(v);
           if (lane < a.R) sh.rr[lane] = v.key ? static_cast<int32_t>(v.uid ^ 0x80000000u) : -1;
         } else {
           for (int r = 0; r < a.R; ++r) {
             Sel best{0u, 0xffffffffu, 0xffffffffu};
-            for (int q = lane; q < total; q += 32) {
-              const Sel v = sh.surv[q];
-              if (v.key != 0u && (best.key == 0u || sel_before(v, best))) best = v;
-            }
+            for (int c = 0; c < kRC; ++c)
+              for (int q = lane; q < sh.rcnt[c]; q += 32) {
+                const Sel v = sh.surv[c * kRCRegion + q];
+                if (v.key != 0u && (best.key == 0u || sel_before(v, best))) best = v;
+              }
             const Sel wb = warp_best(best);
-            for (int q = lane; q < total; q += 32)
-              if (sh.surv[q].key != 0u && sh.surv[q].idx == wb.idx) sh.surv[q].key = 0u;
+            for (int c = 0; c < kRC; ++c)
+              for (int q = lane; q < sh.rcnt[c]; q += 32)
+                if (sh.surv[c * kRCRegion + q].key != 0u && sh.surv[c * kRCRegion + q].idx == wb.idx)
+                  sh.surv[c * kRCRegion + q].key = 0u;
             __syncwarp();
             if (lane == 0) sh.rr[r] = wb.key ? static_cast<int32_t>(wb.uid ^ 0x80000000u) : -1;
           }
         }
       }
     } else {
-      // heavy ties overflowed the list: the exact R-round selection over the whole row
+      // heavy ties overflowed a region: the exact R-round selection over the whole row
       for (int i = tid; i < (a.ncand + 31) / 32; i += kRCThreads) sh.retired[i] = 0u;
       __syncthreads();
       for (int r = 0; r < a.R; ++r) {
@@ -571,21 +582,18 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
       }
     }
     __syncthreads();
-    if (tid < a.R) {
+    if (rank == 0 && tid < a.R) {
       const int32_t id = sh.rr[tid];
       a.rr_id[static_cast<int64_t>(m) * a.R + tid] = id;
       if (a.h_rr_id) a.h_rr_id[static_cast<int64_t>(m) * a.R + tid] = id;
-      for (int c = 1; c < kRC; ++c) cl.map_shared_rank(sh.rr, c)[tid] = id;
     }
   }
-  cl.sync();
 
-  // 5. exact dots of this CTA's slots (rank, rank + kRC, ...): all of a thread's weight loads
+  // 4. exact dots of this CTA's slots (rank, rank + kRC, ...): all of a thread's weight loads
   // for all its slots are in flight together; fixed-order reductions
   {
     const int nslot = (a.R - rank + kRC - 1) / kRC;  // 0..4
     const int k8n = a.K / 8;
-    const uint4* xr = reinterpret_cast<const uint4*>(xs);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int rown[4];
     bool live[4];
@@ -597,6 +605,12 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
     }
     for (int k8b = tid; k8b < k8n; k8b += kRCThreads * 3) {
       typename Row8<FP8>::Raw w8[4][3];
+      uint4 xq[3];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int k8 = k8b + q * kRCThreads;
+        xq[q] = k8 < k8n ? xr[k8] : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -609,7 +623,7 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
       for (int q = 0; q < 3; ++q) {
         const int k8 = k8b + q * kRCThreads;
         if (k8 < k8n) {
-          const uint4 x8 = xr[k8];
+          const uint4 x8 = xq[q];
           const uint32_t xv[4] = {x8.x, x8.y, x8.z, x8.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -650,7 +664,7 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
   }
   cl.sync();
 
-  // 6. CTA 0: outputs and the argmax (ties to the lowest id)
+  // 5. CTA 0: outputs and the argmax (ties to the lowest id)
   if (rank == 0 && warp == 0) {
     uint32_t bk = 0u, bu = 0xffffffffu;
     for (int j = lane; j < a.R; j += 32) {
@@ -678,12 +692,10 @@ __global__ void __cluster_dims__(kRC, 1, 1) __launch_bounds__(kRCThreads, 1)
 
 template <int LPT, bool FP8>
 static cudaError_t launch_rc(const RerankArgs& a, int M, cudaStream_t s) {
-  const int smem = 2 * a.K;
-  cudaError_t e = cudaFuncSetAttribute(rerank_cluster_kernel<LPT, FP8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  // programmatic dependent launch: the CTAs may start (and stage x) while the kernel before
-  // them in the stream finishes; they wait for its completion before reading the candidates
+  const int smem = 0;
+  cudaError_t e = cudaSuccess;
+  // programmatic dependent launch: the CTAs may start (and fetch x into L2) while the kernel
+  // before them in the stream finishes; they wait for its completion before reading anything
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M * kRC);
   cfg.blockDim = dim3(kRCThreads);
