@@ -13,30 +13,31 @@
 //
 // Work decomposition:
 //  * A prep kernel lays the pass's hidden states out as the MMA's B operand in the caller's
-//    workspace: x * 2^(15 - E_m) / 4^p as f16 (E_m from max |x[m]|; plane p's codes are
-//    v * 4^p * 2^-24 as f16 subnormals, so every product is v x 2^(15 - E_m) 2^-24 exactly),
-//    grouped per (scale group J, plane p) into one contiguous unit; also the group sums XS.
+//    workspace: x * 2^(15 - E_m) as f16 (E_m from max |x[m]|), one contiguous unit per (scale
+//    group J, plane p, quarter of the group's chunks); also the group sums XS and the E_m.
 //  * Persistent grid, one CTA per SM, 128-row tiles (the MMA's M = TMEM lanes). One producer
 //    thread feeds two rings without blocking on either: the packed rows through 128 x 128-byte
 //    stages with 2-D tensor-map copies (TMA, 128-byte swizzle), and the B operand through
-//    half-units (half of a (scale group, plane)'s chunks) with bulk copies.
+//    quarter slots (the four plane units of a quarter: four bulk copies, one barrier).
 //  * 8 dequantising warps, two per TMEM lane quadrant (even and odd chunks); the thread of TMEM
-//    lane r owns row r. A 16-byte chunk of its row (16 byte positions x 4 planes) becomes 32
-//    registers of f16 pairs with one AND each (the odd bytes come down by one shift per word),
-//    written to a 32-column TMEM A stage by one tcgen05.st: plane p's 16 codes are the stage's
-//    columns 8p .. 8p + 7.
-//  * Four MMA-issuing threads (warps 1 .. 4), one per plane: independent accumulation chains
-//    keep the tensor pipe busy (one thread issues an MMA only every ~100 ns). Plane p of scale
-//    group J accumulates the group's chunks into D slot p (128 x N fp32), so the page's
-//    per-group scale is applied to the accumulator, never to the weight tile:
-//    acc += S[n, g] * D_g. The zero-point part sum_g (S - ZS) XS_g (the page's
-//    S (XS + sum x v / 4) - ZS XS rearranged) is a per-row dot with the group sums. A stage is
-//    released when all four issuers' MMAs on it are done, a B half-unit when its issuer's are.
-//  * 8 fold warps (two per TMEM lane quadrant, half of the columns each; thread = row) read
-//    each D slot as soon as its group is complete, release it to its issuer, and add
-//    S_g D_g + (S_g - ZS_g) XS_g into registers; then they hand the tile's keys to 3 selection
-//    warps, which pick the top-KCAND of each 64-row block per hidden row (warp reductions on
-//    order-preserving keys, lowest row on ties).
+//    lane r owns row r and, per tile, the exponent e of its largest scale (S 2^e in [8, 16)).
+//    A 16-byte chunk of its row (16 byte positions x 4 planes) becomes 32 registers of f16
+//    pairs: per word and plane one LOP3 puts the two codes c (times 4^p) into the mantissa of
+//    1.0, and one HFMA2 with the pair (M, -M), M = S 2^(e + 10 - 2p), leaves exactly c S 2^e
+//    (one rounding of a product with at most 10 significant bits). One tcgen05.st writes the
+//    chunk's 32-column A stage: plane p's 16 codes are the stage's columns 8p .. 8p + 7.
+//  * Three MMA-issuing threads (warps 1 .. 3): B quarter Q of the pass goes to issuer Q mod 3,
+//    which accumulates all its quarters of the tile (every chunk and plane: the scale is in the
+//    A operand) into its own D slot (128 x N fp32). A quarter's B slot and A stages belong to
+//    its issuer alone: one wait for each and one commit releasing each per quarter, since one
+//    thread issues an MMA only every ~100 ns and bookkeeping on that thread costs MMAs.
+//  * 8 fold warps (two per TMEM lane quadrant, half of the columns each; thread = row) form the
+//    zero-point part sum_g (S_g - ZS_g) XS_g while the tile's MMAs run, then add the three D
+//    slots times 2^(E_m - e - 17), which is sum_g S_g sum x c / 4: together the page's
+//    S (XS + sum x v / 4) - ZS XS summed over the groups. The tile's keys go to a per-CTA
+//    column-major buffer in the workspace; the fold warps and 3 selection warps split the
+//    top-KCAND of each 64-row block per hidden row (warp reductions on order-preserving keys,
+//    lowest row on ties).
 // Every wait is bounded (kWaitLimitNs); a wait that runs out marks the launch failed in the
 // status word, after which every wait returns at once and the kernel runs to its end.
 #include <cuda.h>
@@ -59,8 +60,9 @@ constexpr int kWStageSmem = kWRows * kWStageBytes;
 constexpr int kWDeqWarps = 8;   // dequantising: two per TMEM lane quadrant
 constexpr int kWFoldWarps = 8;  // fold: two per TMEM lane quadrant
 constexpr int kWSelWarps = 3;   // block top-KCAND selection (off the critical path)
-constexpr int kWIssuers = 4;    // MMA-issuing threads: one per int2 plane
-// warp 0: the copy producer (one thread, both rings); warps 1 .. 4: the MMA issuers; then the
+constexpr int kWSelWorkers = kWSelWarps + kWFoldWarps;  // the fold warps take a share too
+constexpr int kWIssuers = 3;    // MMA-issuing threads: chunk c goes to issuer c % 3
+// warp 0: the copy producer (one thread, both rings); warps 1 .. 3: the MMA issuers; then the
 // dequantising, fold and selection warps
 constexpr int kWDeq0 = 1 + kWIssuers;          // first dequantising warp
 constexpr int kWFold0 = kWDeq0 + kWDeqWarps;   // first fold warp
@@ -68,7 +70,8 @@ constexpr int kWSel0 = kWFold0 + kWFoldWarps;  // first selection warp
 constexpr int kWWarps = kWSel0 + kWSelWarps;
 constexpr int kWThreads = kWWarps * 32;
 constexpr int kWMaxNP = 8;   // packed ring stages at most
-constexpr int kWNB = 8;      // B ring: two half-units per issuer
+constexpr int kWNB = 6;      // B ring slots: a quarter of a scale group each (four plane units)
+constexpr int kWMaxGrid = 256;  // CTAs of a pass the per-CTA key buffers are sized for
 constexpr int kWMaxNA = 14;  // A stages at most (32 TMEM columns each)
 constexpr int kWTmemCols = 512;
 constexpr int kWPrepThreads = 256;
@@ -88,6 +91,7 @@ struct WideArgs {
   uint16_t* y;  // bf16 [M, N] or nullptr
   uint32_t* status;
   int np, nbu, unit_bytes, szp;
+  uint32_t* keys_g;  // per-CTA key buffers [grid][128][NCOL] (scratch)
   int off_bring, off_sz, off_keys, off_xs, off_ew, off_bars;
 };
 
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kWPrepThreads) wide_prep_kernel(const uint16_t
     if (live) {
       const int k0 = p * RB + 16 * (J * CPJ + cj) + 8 * h;
       const uint4 v = *reinterpret_cast<const uint4*>(xr + k0);
-      const float sx = w_pow2(15 - e - 2 * p);
+      const float sx = w_pow2(15 - e);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t hv[8];
 #pragma unroll
@@ -172,20 +176,23 @@ __global__ void __launch_bounds__(kWPrepThreads) wide_prep_kernel(const uint16_t
 template <int G, int NCOL>
 __global__ void __launch_bounds__(kWThreads, 1)
     coarse_wide_kernel(const __grid_constant__ CUtensorMap tmap, const WideArgs a) {
-  constexpr int P = 4;           // int2 planes
-  constexpr int CPJ = G / 16;    // chunks per scale group
-  constexpr int CPH = CPJ / 2;   // chunks per B half-unit
-  constexpr int ACOLS = 32;      // TMEM columns of one A stage: one chunk, four planes
-  // Four D slots (one per plane) at columns 0 .. 4 NCOL, then the A stages, an even number (the
-  // two dequantising parities own alternate stages)
-  constexpr int NAS = ((kWTmemCols - 4 * NCOL) / ACOLS > kWMaxNA ? kWMaxNA
-                                                                   : (kWTmemCols - 4 * NCOL) / ACOLS) &
+  constexpr int P = 4;                       // int2 planes
+  constexpr int CPJ = G / 16;                // chunks per scale group
+  constexpr int CPQ = CPJ / 4;               // chunks per B quarter-unit
+  constexpr int ACOLS = 32;                  // TMEM columns of one A stage: one chunk, four planes
+  // kWIssuers D slots (one per issuer, a whole tile each) at columns 0 .. kWIssuers NCOL, then the
+  // A stages, an even number (the two dequantising parities own alternate stages)
+  constexpr int NAS = ((kWTmemCols - kWIssuers * NCOL) / ACOLS > kWMaxNA
+                           ? kWMaxNA
+                           : (kWTmemCols - kWIssuers * NCOL) / ACOLS) &
                       ~1;
-  constexpr int PITCH = NCOL + 1;  // words per row of the key buffer (odd: no bank conflicts)
+  constexpr int NAQ = NAS / CPQ;  // A ring in quarters (the issuers' unit of work)
+  constexpr int PITCH = NCOL;  // key buffer: [NCOL][128] words per CTA
   constexpr int HC = NCOL / 2;     // D columns of one fold warp
   static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 80, "MMA N");
   static_assert(NAS >= 2, "TMEM budget: at least one A stage per dequantising parity");
-  static_assert(CPH >= 1 && CPJ % 2 == 0, "B half-units");
+  static_assert(NAS % CPQ == 0 && NAQ >= 2, "A ring: whole quarters, at least two");
+  static_assert(CPQ >= 1 && CPJ == 4 * CPQ, "four B quarter-units per (group, plane)");
   extern __shared__ unsigned char sm_raw[];
   // 1024-byte alignment for the 128-byte swizzle of the packed ring
   unsigned char* sm = sm_raw + ((1024u - (smem_addr(sm_raw) & 1023u)) & 1023u);
@@ -194,13 +201,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const int np = a.np;
   uint64_t* pfull = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kWMaxNP] stage landed
   uint64_t* pempty = pfull + kWMaxNP;   // [kWMaxNP] stage read by the dequantising warps
-  uint64_t* bfull = pempty + kWMaxNP;   // [kWNB] B half-unit landed
-  uint64_t* bempty = bfull + kWNB;      // [kWNB] B half-unit's MMAs done
+  uint64_t* bfull = pempty + kWMaxNP;   // [kWNB] B quarter landed (four plane units)
+  uint64_t* bempty = bfull + kWNB;      // [kWNB] every issuer past the quarter
   uint64_t* afull = bempty + kWNB;      // [kWMaxNA] A stage written
-  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA] A stage's MMAs (all four issuers) done
-  uint64_t* dfull = aempty + kWMaxNA;   // [4] D slot p complete for the group
-  uint64_t* dempty = dfull + 4;         // [4] D slot p read by the fold warps
-  uint64_t* mma_done = dempty + 4;      // every MMA of the CTA complete
+  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA] A stage's MMAs done
+  uint64_t* dfull = aempty + kWMaxNA;   // the tile's D slots complete
+  uint64_t* dempty = dfull + 1;         // ... and read by the fold warps
+  uint64_t* mma_done = dempty + 1;      // every MMA of the CTA complete
   uint64_t* keys_ready = mma_done + 1;  // a tile's keys written by the fold warps
   uint64_t* keys_free = mma_done + 2;   // ... and consumed by the selection warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 3);
@@ -210,8 +217,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       (a.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
       static_cast<int>(gridDim.x);
   const int total_stages = my_tiles * a.NS;
-  const int halves_per_tile = a.NJ * P * 2;
-  const int total_halves = my_tiles * halves_per_tile;
+  const int quarters_per_tile = a.NJ * 4;  // B quarters of a tile: 4 per group
+  const int total_quarters = my_tiles * quarters_per_tile;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWMaxNP; ++i) {
@@ -220,19 +227,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
     for (int i = 0; i < kWNB; ++i) {
       mbar_init(&bfull[i], 1u);
-      mbar_init(&bempty[i], 1u);  // its issuer's commit
+      mbar_init(&bempty[i], 1u);  // the quarter's issuer
     }
     for (int i = 0; i < kWMaxNA; ++i) {
-      mbar_init(&afull[i], 4u);   // the 4 quadrant warps of the stage's chunk parity
-      mbar_init(&aempty[i], static_cast<uint32_t>(kWIssuers));  // one commit per issuer
+      mbar_init(&afull[i], 4u * CPQ);  // the quadrant warps of the quarter's chunks
+      mbar_init(&aempty[i], 1u);        // the quarter's issuer
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&dfull[i], 1u);   // the slot's issuer
-      mbar_init(&dempty[i], static_cast<uint32_t>(kWFoldWarps));
-    }
+    mbar_init(dfull, static_cast<uint32_t>(kWIssuers));
+    mbar_init(dempty, static_cast<uint32_t>(kWFoldWarps));
     mbar_init(mma_done, static_cast<uint32_t>(kWIssuers));
     mbar_init(keys_ready, static_cast<uint32_t>(kWFoldWarps));
-    mbar_init(keys_free, static_cast<uint32_t>(kWSelWarps));
+    mbar_init(keys_free, static_cast<uint32_t>(kWSelWorkers));
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_map(&tmap);
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_base = tmem + 4 * NCOL;  // column of A stage 0 (D slot p at p NCOL)
+  const uint32_t a_base = tmem + kWIssuers * NCOL;  // column of A stage 0 (D slot q at q NCOL)
 
   // Bounded wait on one phase of an mbarrier: one test first (the common case costs one
   // instruction and no clock read), then suspended waits. Returns at once (false) once the launch
@@ -270,6 +275,79 @@ __global__ void __launch_bounds__(kWThreads, 1)
       ph ^= 1u;
     }
   };
+  // the row's scale exponent: S 2^e in [8, 16) for the row's largest S (bf16 magnitude bits)
+  auto scale_exponent = [](uint32_t max_bits) {
+    return max_bits ? 130 - static_cast<int>(max_bits >> 7) : 0;
+  };
+
+  // block top-KCAND of this worker's share of a tile's jobs (job j = (64-row block j / R of the
+  // tile, hidden row j % R)), from the tile's keys [128][PITCH]; a warp runs JB jobs at once so
+  // that their warp reductions overlap (each round of one job is a chain of two)
+  auto select_jobs = [&](int worker, int tile, const uint32_t* keys) {
+    constexpr int JB = 4;
+    for (int j0 = worker * JB; j0 < 2 * a.R; j0 += kWSelWorkers * JB) {
+      uint32_t k0[JB], k1[JB], key_lo[JB], row_lo[JB], key_hi[JB], row_hi[JB];
+      int bb[JB], mm[JB];
+#pragma unroll
+      for (int u = 0; u < JB; ++u) {
+        const int jj = j0 + u;
+        const int blk = jj / a.R;
+        mm[u] = jj - blk * a.R;
+        bb[u] = tile * 2 + blk;
+        const bool live = jj < 2 * a.R && bb[u] < a.nblk;
+        const uint32_t* kc = keys + mm[u] * kWRows + 64 * blk;
+        k0[u] = live ? __ldcg(kc + lane) : 0u;  // L2: this CTA wrote them just before
+        k1[u] = live ? __ldcg(kc + lane + 32) : 0u;
+        key_lo[u] = key_hi[u] = 0u;  // slots lane, lane + 32
+        row_lo[u] = row_hi[u] = 64u;
+        if (!live) bb[u] = -1;
+      }
+      for (int r = 0; r < a.kcand; ++r) {
+        uint32_t bk[JB], brow[JB], kmax[JB], rwin[JB];
+#pragma unroll
+        for (int u = 0; u < JB; ++u) {
+          const bool first = k0[u] >= k1[u];
+          bk[u] = first ? k0[u] : k1[u];
+          brow[u] = first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
+          kmax[u] = __reduce_max_sync(0xffffffffu, bk[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < JB; ++u)
+          rwin[u] = __reduce_min_sync(0xffffffffu, bk[u] == kmax[u] ? brow[u] : 64u);
+#pragma unroll
+        for (int u = 0; u < JB; ++u) {
+          if (kmax[u] != 0u && lane == static_cast<int>(rwin[u] & 31u)) {
+            if (rwin[u] < 32u) k0[u] = 0u; else k1[u] = 0u;
+          }
+          if (lane == (r & 31)) {
+            if (r < 32) {
+              key_lo[u] = kmax[u];
+              row_lo[u] = kmax[u] ? rwin[u] : 64u;
+            } else {
+              key_hi[u] = kmax[u];
+              row_hi[u] = kmax[u] ? rwin[u] : 64u;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < JB; ++u) {
+        if (bb[u] < 0) continue;
+        const int b = bb[u];
+        const int64_t obase = static_cast<int64_t>(a.m0 + mm[u]) * a.nblk * a.kcand +
+                              static_cast<int64_t>(b) * a.kcand;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int slot = lane + 32 * h;
+          const uint32_t kk = h ? key_hi[u] : key_lo[u], rr = h ? row_hi[u] : row_lo[u];
+          if (slot < a.kcand) {
+            a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
+            a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
+          }
+        }
+      }
+    }
+  };
 
   int issued = 0, issued_b = 0;  // copies issued into the packed and B rings (warp 0, lane 0)
   if (warp == 0) {
@@ -284,7 +362,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int pslot = 0, ps_in_tile = 0, plt = 0, bslot = 0, bunit = 0;
       uint32_t pph = 0u, bph = 0u;
       uint64_t t_idle = 0;
-      while ((issued < total_stages || issued_b < total_halves) && !*abort_flag) {
+      while ((issued < total_stages || issued_b < total_quarters) && !*abort_flag) {
         bool progress = false;
         if (issued < total_stages &&
             (issued < np || mbar_test_wait(&pempty[pslot], pph ^ 1u))) {
@@ -299,17 +377,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
           ++issued;
           progress = true;
         }
-        if (issued_b < total_halves &&
+        if (issued_b < total_quarters &&
             (issued_b < kWNB || mbar_test_wait(&bempty[bslot], bph ^ 1u))) {
-          // a group's half-units go out first halves first, plane by plane, so that the four
-          // issuers get theirs together: unit (J, h, p) of the order is (J, p, h) of the layout
-          const int uj = bunit >> 3, uh = (bunit >> 2) & 1, up = bunit & 3;
-          mbar_arrive_expect_tx(&bfull[bslot], static_cast<uint32_t>(a.unit_bytes));
-          bulk_g2s(sm + a.off_bring + bslot * a.unit_bytes,
-                   a.bbuf + static_cast<int64_t>((uj * 4 + up) * 2 + uh) * a.unit_bytes,
-                   static_cast<uint32_t>(a.unit_bytes), &bfull[bslot]);
+          // quarter (J, uq): the prep layout is (J, plane, chunk), so the quarter is four
+          // contiguous plane units, one copy each, landing side by side in the slot
+          const int uj = bunit >> 2, uq = bunit & 3;
+          mbar_arrive_expect_tx(&bfull[bslot], static_cast<uint32_t>(P * a.unit_bytes));
+#pragma unroll
+          for (int up = 0; up < P; ++up)
+            bulk_g2s(sm + a.off_bring + (bslot * P + up) * a.unit_bytes,
+                     a.bbuf + static_cast<int64_t>((uj * 4 + up) * 4 + uq) * a.unit_bytes,
+                     static_cast<uint32_t>(a.unit_bytes), &bfull[bslot]);
           advance(bslot, bph, kWNB);
-          if (++bunit == halves_per_tile) bunit = 0;
+          if (++bunit == quarters_per_tile) bunit = 0;
           ++issued_b;
           progress = true;
         }
@@ -329,52 +409,60 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
     __syncwarp();
   } else if (warp <= kWIssuers) {
-    // ---- MMA issue: issuer p = warp - 1 takes plane p of every scale group: the group's chunks
-    // into D slot p, A from the chunk's stage (columns 8p .. 8p + 7), B from its two half-units
-    // (ring slots p and 4 + p, one phase per group). Descriptors and ring positions move by
-    // additions only.
-    const int p = warp - 1;
+    // ---- MMA issue: issuer q = warp - 1 takes the B quarters Q == q (mod 3) of the pass, all
+    // chunks and planes of each (the scale is in the A operand, so every plane and group of the
+    // tile accumulates into the issuer's one D slot). A B slot (Q mod 6) and an A quarter slot
+    // always belong to one issuer, which alone waits for and releases them.
+    const int q = warp - 1;
     if (lane == 0) {
       const uint32_t idesc = tc_idesc_f16(kWRows, NCOL);
       const uint64_t bdesc0 = tc_sdesc(smem_addr(sm + a.off_bring), NCOL * 16, 128u);
-      const uint32_t d = tmem + p * NCOL, a_col = a_base + 8 * p;
-      uint32_t bph = 0u;
-      int as = 0;
-      uint32_t aph = 0u;
-      int grp = 0;  // groups issued
+      const uint32_t d = tmem + q * NCOL;
+      int aq = 0, bslot = 0;
+      uint32_t aph = 0u, bph = 0u;
+      int rq = 0;  // quarter index of the pass mod 3
       for (int lt = 0; lt < my_tiles; ++lt) {
-        for (int J = 0; J < a.NJ; ++J, ++grp) {
-          if (grp > 0) wait_bar(&dempty[p], static_cast<uint32_t>(grp - 1) & 1u);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int bslot = 4 * hh + p;
-            wait_bar(&bfull[bslot], bph);
-            tc_fence_after();
-            const uint64_t bd = bdesc0 + static_cast<uint64_t>((bslot * a.unit_bytes) >> 4);
-#pragma unroll 2
-            for (int cj = 0; cj < CPH; ++cj) {
-              wait_bar(&afull[as], aph);
+        if (lt > 0) wait_bar(dempty, static_cast<uint32_t>(lt - 1) & 1u);
+        bool first = true;  // the issuer's first MMA of the tile starts its D slot
+        for (int J = 0; J < a.NJ; ++J) {
+          for (int qq = 0; qq < 4; ++qq) {
+            if (rq == q) {
+              wait_bar(&bfull[bslot], bph);  // the quarter's four plane units
+              wait_bar(&afull[aq], aph);     // its chunks' A stages
               tc_fence_after();
-              tc_mma_f16_ts(d, a_col + as * ACOLS,
-                            bd + static_cast<uint64_t>((cj * 2 * NCOL * 16) >> 4), idesc,
-                            (hh | cj) != 0);
-              tc_commit(&aempty[as]);
-              advance(as, aph, NAS);
+#pragma unroll
+              for (int cc = 0; cc < CPQ; ++cc) {
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                  const uint64_t bd =
+                      bdesc0 + static_cast<uint64_t>(
+                                   ((bslot * P + p) * a.unit_bytes + cc * 2 * NCOL * 16) >> 4);
+                  tc_mma_f16_ts(d, a_base + (aq * CPQ + cc) * ACOLS + 8 * p, bd, idesc,
+                                !(first && cc == 0 && p == 0));
+                }
+              }
+              first = false;
+              tc_commit(&aempty[aq]);
+              tc_commit(&bempty[bslot]);
             }
-            tc_commit(&bempty[bslot]);  // the half-unit's MMAs done: the producer may refill it
+            advance(aq, aph, NAQ);
+            advance(bslot, bph, kWNB);
+            if (++rq == kWIssuers) rq = 0;
           }
-          tc_commit(&dfull[p]);
-          bph ^= 1u;
         }
+        tc_commit(dfull);
       }
       tc_commit(mma_done);
       mbar_wait_bounded(mma_done, 0u);  // also after an abort: no MMA may outlive the TMEM
     }
     __syncwarp();
   } else if (warp < kWFold0) {
-    // ---- dequantisation: eight warps, two per TMEM lane quadrant (one for the even chunks of a
-    // group, one for the odd), one thread per row. A stage holds one chunk's four planes
-    // (32 columns) of 16 byte positions as f16 pairs (one AND each).
+    // ---- dequantisation: eight warps, two per TMEM lane quadrant (one for the even chunks, one
+    // for the odd), one thread per row. A stage holds one chunk's four planes (32 columns) of 16
+    // byte positions as f16 pairs c S 2^e: per pair one LOP3 puts the two codes (times 4^p) into
+    // the mantissa of 1.0, one HFMA2 with the group's multiplier M = S 2^(e + 10 - 2p) and -M
+    // leaves exactly c S 2^e (the FMA rounds once, and the product has at most 10 significant
+    // bits).
     const int sub = (warp - kWDeq0) >> 2;  // chunk parity of this warp
     const int row = (warp & 3) * 32 + lane;
     const uint32_t my_a = a_base + tmem_lane_base(warp);
@@ -384,20 +472,55 @@ __global__ void __launch_bounds__(kWThreads, 1)
     int as = sub;  // A ring slot of this warp's next chunk (the parities alternate: NAS is even)
     uint32_t aph = 0u;
     int done0 = 0;  // chunks of the pass before the current group
+    grid_dependency_wait();  // the scales may be the preceding kernel's output (the quantiser)
     for (int lt = 0; lt < my_tiles; ++lt) {
+      const int n = tile_of(lt) * kWRows + row;
+      const uint16_t* srow = a.S + static_cast<int64_t>(n < a.N ? n : 0) * a.KG;
+      if (lt + 1 < my_tiles) {  // the next tile's scale row heads for L2
+        const int n1 = tile_of(lt + 1) * kWRows + row;
+        if (n1 < a.N)
+          prefetch_l2_bulk(a.S + static_cast<int64_t>(n1) * a.KG, static_cast<uint32_t>(a.KG * 2));
+      }
+      // the row's largest S: every 16-byte load of the row in flight together (K/G <= 80)
+      uint32_t mx = 0u;
+      {
+        uint4 v[10];
+#pragma unroll
+        for (int i = 0; i < 10; ++i)
+          v[i] = i < a.KG / 8 ? reinterpret_cast<const uint4*>(srow)[i] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < 10; ++i) {
+          const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+        }
+      }
+      const int en = scale_exponent(mx);
+      // the four planes' S of a group, loaded one group ahead
+      uint32_t snext[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) snext[p] = srow[p * a.NJ];
       for (int J = 0; J < a.NJ; ++J) {
         const int c0 = J * CPJ;  // the group's first chunk within the tile
-        if ((c0 & 7) == 0) {     // the group starts a packed stage (8 chunks)
+        // plane p's multiplier pair (M, -M) as f16x2
+        uint32_t mul[P], bias[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          const float sv = bf16_bits_to_float(snext[p]) * w_pow2(en + 10 - 2 * p);
+          const uint32_t hm = __half_as_ushort(__float2half_rn(sv));
+          mul[p] = hm | (hm << 16);
+          bias[p] = mul[p] ^ 0x80008000u;
+        }
+        if (J + 1 < a.NJ) {
+#pragma unroll
+          for (int p = 0; p < P; ++p) snext[p] = srow[p * a.NJ + J + 1];
+        }
+        if ((c0 & 7) == 0) {  // the group starts a packed stage (8 chunks)
           wait_bar(&pfull[ps], pph);
           __syncwarp();
         }
         const unsigned char* prow = sm + ps * kWStageSmem + row * kWStageBytes;
         for (int cj = sub; cj < CPJ; cj += 2) {
-          if (done0 + cj >= NAS) {  // the stage's previous MMAs are done
-            wait_bar(&aempty[as], aph ^ 1u);
-            __syncwarp();
-          }
-          tc_fence_after();
           const int c = c0 + cj;
           const uint4 w4 = *reinterpret_cast<const uint4*>(prow + ((((c & 7) ^ sw)) << 4));
           const uint32_t t[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -406,17 +529,32 @@ __global__ void __launch_bounds__(kWThreads, 1)
           for (int w = 0; w < 4; ++w) {
             const uint32_t te = t[w], to = t[w] >> 8;
 #pragma unroll
-            for (int q = 0; q < P; ++q) {
-              const uint32_t mk = 0x00030003u << (2 * q);
-              r[8 * q + 2 * w] = te & mk;
-              r[8 * q + 2 * w + 1] = to & mk;
+            for (int p = 0; p < P; ++p) {
+              const uint32_t mk = 0x00030003u << (2 * p);
+              r[8 * p + 2 * w] = (te & mk) | 0x3C003C00u;
+              r[8 * p + 2 * w + 1] = (to & mk) | 0x3C003C00u;
             }
           }
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __half2 h = __hfma2(*reinterpret_cast<const __half2*>(&r[8 * p + i]),
+                                        *reinterpret_cast<const __half2*>(&mul[p]),
+                                        *reinterpret_cast<const __half2*>(&bias[p]));
+              r[8 * p + i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+          }
+          if (done0 + cj >= NAS) {  // the stage's previous MMAs are done
+            wait_bar(&aempty[as / CPQ], aph ^ 1u);
+            __syncwarp();
+          }
+          tc_fence_after();
           tmem_st_x32(my_a + as * ACOLS, r);
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[as]);
+          if (lane == 0) mbar_arrive(&afull[as / CPQ]);
           as += 2;
           if (as >= NAS) {
             as -= NAS;
@@ -432,7 +570,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
       }
     }
   } else if (warp < kWSel0) {
-    // ---- fold: two warps per TMEM lane quadrant, each NCOL/2 columns of its 32 rows ------------
+    // ---- fold: two warps per TMEM lane quadrant, each NCOL/2 columns of its 32 rows. While the
+    // tile's MMAs run, the zero-point part sum_g (S_g - ZS_g) XS_g; then the three D slots
+    // (sum_g S_g sum x v times 2^(e + 15 - E_m)) in logit units added to it.
     const int fw = warp - kWFold0;  // 0..7
     const int half = fw >> 2;
     const int row = (warp & 3) * 32 + lane;
@@ -440,7 +580,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const uint32_t my_d = tmem + tmem_lane_base(warp) + col0;
     unsigned char* s_row = sm + a.off_sz + row * a.szp;  // this row's S ...
     unsigned char* z_row = s_row + kWRows * a.szp;       // ... and ZS
-    uint32_t* keys = reinterpret_cast<uint32_t*>(sm + a.off_keys);  // [128][PITCH]
+    // this CTA's key buffer [128][PITCH] in global memory (L2): written here, read by the
+    // selection warps through L2
+    uint32_t* keys = a.keys_g + static_cast<int64_t>(blockIdx.x) * kWRows * PITCH;
     float* xsd = reinterpret_cast<float*>(sm + a.off_xs);           // [KG][NCOL]
     int* ew_s = reinterpret_cast<int*>(sm + a.off_ew);              // [NCOL]
     // the half-0 warp copies the row's S, the half-1 warp its ZS; a barrier of the fold warps
@@ -462,20 +604,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
         prefetch_l2_bulk((half ? a.ZS : a.S) + static_cast<int64_t>(n) * a.KG,
                          static_cast<uint32_t>(a.KG * 2));
     }
-    // the prep kernel's group sums and exponents (the outputs are written after this wait
-    // too): XS in the units of the D slots, 2^24 / (2^(15 - E_m) 4) = 2^(E_m + 7), as
-    // xsd[g][m] = XS[m][g] 2^-(E_m + 7) (a power of two: exact)
+    // the prep kernel's group sums and exponents (the outputs are written after this wait too):
+    // xsd[g][m] = XS[m][g]
     grid_dependency_wait();
     if (my_tiles > 0) load_sz(0);
     const int ftid = fw * 32 + lane;
     if (ftid < NCOL) ew_s[ftid] = a.ew[ftid];
     for (int i = ftid; i < NCOL * a.KG; i += kWFoldWarps * 32) {
       const int m = i / a.KG, gi = i - m * a.KG;
-      xsd[gi * NCOL + m] = a.xs[i] * w_pow2(-(a.ew[m] + 7));
+      xsd[gi * NCOL + m] = a.xs[i];
     }
     named_bar_sync(2, kWFoldWarps * 32);
-    int grp = 0;
-    constexpr int kBatch = 24;  // D columns loaded per wait (three 8-column loads)
+    constexpr int kBatch = 8;  // D columns per load, three slots per wait
     for (int lt = 0; lt < my_tiles; ++lt) {
       const int n = tile_of(lt) * kWRows + row;
       const bool valid = n < a.N;
@@ -484,46 +624,45 @@ __global__ void __launch_bounds__(kWThreads, 1)
       float acc[HC];
 #pragma unroll
       for (int m = 0; m < HC; ++m) acc[m] = 0.0f;
-      // the group's D slots as their issuers complete them; each adds S_g D_g and the
-      // zero-point part (S_g - ZS_g) XS_g, and goes back to its issuer once read
-      for (int J = 0; J < a.NJ; ++J, ++grp) {
-        for (int p = 0; p < P; ++p) {
-          const int gi = p * a.NJ + J;
-          wait_bar(&dfull[p], static_cast<uint32_t>(grp) & 1u);
-          __syncwarp();
-          tc_fence_after();
-          const float sg = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(s_row + 2 * gi));
-          const float zg = sg - bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(z_row + 2 * gi));
-          const float4* xg4 = reinterpret_cast<const float4*>(xsd + gi * NCOL + col0);
+      uint32_t mx = 0u;
+      for (int gi = 0; gi < a.KG; ++gi) {
+        const uint32_t sb = *reinterpret_cast<const uint16_t*>(s_row + 2 * gi);
+        mx = max(mx, sb & 0x7fffu);
+        const float zg = bf16_bits_to_float(sb) -
+                         bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(z_row + 2 * gi));
+        const float4* xg4 = reinterpret_cast<const float4*>(xsd + gi * NCOL + col0);
 #pragma unroll
-          for (int q0 = 0; q0 < HC; q0 += kBatch) {
-            constexpr int kB = kBatch;
-            uint32_t dv[kB];
-#pragma unroll
-            for (int q = 0; q < kB; q += 8)
-              if (q0 + q < HC) tmem_ld<8>(my_d + p * NCOL + q0 + q, dv + q);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < kB; q += 4) {
-              if (q0 + q < HC) {
-                const float4 x4 = xg4[(q0 + q) >> 2];
-                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  acc[q0 + q + i] =
-                      fmaf(sg, __uint_as_float(dv[q + i]), fmaf(zg, xv[i], acc[q0 + q + i]));
-              }
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&dempty[p]);
+        for (int q = 0; q < HC; q += 4) {
+          const float4 x4 = xg4[q >> 2];
+          acc[q] = fmaf(zg, x4.x, acc[q]);
+          acc[q + 1] = fmaf(zg, x4.y, acc[q + 1]);
+          acc[q + 2] = fmaf(zg, x4.z, acc[q + 2]);
+          acc[q + 3] = fmaf(zg, x4.w, acc[q + 3]);
         }
       }
+      const int en = scale_exponent(mx);
+      wait_bar(dfull, static_cast<uint32_t>(lt) & 1u);
+      __syncwarp();
+      tc_fence_after();
+#pragma unroll
+      for (int q0 = 0; q0 < HC; q0 += kBatch) {
+        uint32_t d0[kBatch], d1[kBatch], d2[kBatch];
+        tmem_ld<8>(my_d + q0, d0);
+        tmem_ld<8>(my_d + NCOL + q0, d1);
+        tmem_ld<8>(my_d + 2 * NCOL + q0, d2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const float dsum = (__uint_as_float(d0[i]) + __uint_as_float(d1[i])) +
+                             __uint_as_float(d2[i]);
+          acc[q0 + i] = fmaf(dsum, w_pow2(ew_s[col0 + q0 + i] - en - 17), acc[q0 + i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);  // the D slots go back to the issuers
       named_bar_sync(2, kWFoldWarps * 32);  // both halves are done with the tile's S and ZS rows
       if (lt + 1 < my_tiles) load_sz(lt + 1);
-#pragma unroll
-      for (int m = 0; m < HC; ++m) acc[m] *= w_pow2(ew_s[col0 + m] + 7);  // logit units
       if (a.y != nullptr && valid) {
 #pragma unroll
         for (int m = 0; m < HC; ++m)
@@ -536,84 +675,26 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (lt > 0) wait_bar(keys_free, static_cast<uint32_t>(lt - 1) & 1u);
       __syncwarp();
 #pragma unroll
-      for (int m = 0; m < HC; ++m) keys[row * PITCH + col0 + m] = valid ? order_key(acc[m]) : 0u;
+      for (int m = 0; m < HC; ++m) keys[(col0 + m) * kWRows + row] = valid ? order_key(acc[m]) : 0u;
       __syncwarp();
       if (lane == 0) mbar_arrive(keys_ready);
+      // the fold warps are idle until the next tile's D slots fill: they take a share of the
+      // tile's selection jobs once every fold warp's keys are written
+      named_bar_sync(2, kWFoldWarps * 32);
+      select_jobs(kWSelWarps + fw, tile_of(lt), keys);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(keys_free);
     }
   } else {
     // ---- selection: block top-KCAND of every (64-row block, hidden row) of a tile -------------
     grid_dependency_wait();  // the outputs
     const int sw4 = warp - kWSel0;  // 0 .. kWSelWarps - 1
-    const uint32_t* keys = reinterpret_cast<const uint32_t*>(sm + a.off_keys);
+    const uint32_t* keys = a.keys_g + static_cast<int64_t>(blockIdx.x) * kWRows * PITCH;
     for (int lt = 0; lt < my_tiles; ++lt) {
       const int tile = tile_of(lt);
       wait_bar(keys_ready, static_cast<uint32_t>(lt) & 1u);
       __syncwarp();
-      // job j = (64-row block j / R of the tile, hidden row j % R); a warp runs JB jobs at once
-      // so that their warp reductions overlap (each round of one job is a chain of two)
-      constexpr int JB = 4;
-      for (int j0 = sw4 * JB; j0 < 2 * a.R; j0 += kWSelWarps * JB) {
-        uint32_t k0[JB], k1[JB], key_lo[JB], row_lo[JB], key_hi[JB], row_hi[JB];
-        int bb[JB], mm[JB];
-#pragma unroll
-        for (int u = 0; u < JB; ++u) {
-          const int jj = j0 + u;
-          const int blk = jj / a.R;
-          mm[u] = jj - blk * a.R;
-          bb[u] = tile * 2 + blk;
-          const bool live = jj < 2 * a.R && bb[u] < a.nblk;
-          const uint32_t* kc = keys + 64 * blk * PITCH + mm[u];
-          k0[u] = live ? kc[lane * PITCH] : 0u;
-          k1[u] = live ? kc[(lane + 32) * PITCH] : 0u;
-          key_lo[u] = key_hi[u] = 0u;  // slots lane, lane + 32
-          row_lo[u] = row_hi[u] = 64u;
-          if (!live) bb[u] = -1;
-        }
-        for (int r = 0; r < a.kcand; ++r) {
-          uint32_t bk[JB], brow[JB], kmax[JB], rwin[JB];
-#pragma unroll
-          for (int u = 0; u < JB; ++u) {
-            const bool first = k0[u] >= k1[u];
-            bk[u] = first ? k0[u] : k1[u];
-            brow[u] = first ? static_cast<uint32_t>(lane) : static_cast<uint32_t>(lane + 32);
-            kmax[u] = __reduce_max_sync(0xffffffffu, bk[u]);
-          }
-#pragma unroll
-          for (int u = 0; u < JB; ++u)
-            rwin[u] = __reduce_min_sync(0xffffffffu, bk[u] == kmax[u] ? brow[u] : 64u);
-#pragma unroll
-          for (int u = 0; u < JB; ++u) {
-            if (kmax[u] != 0u && lane == static_cast<int>(rwin[u] & 31u)) {
-              if (rwin[u] < 32u) k0[u] = 0u; else k1[u] = 0u;
-            }
-            if (lane == (r & 31)) {
-              if (r < 32) {
-                key_lo[u] = kmax[u];
-                row_lo[u] = kmax[u] ? rwin[u] : 64u;
-              } else {
-                key_hi[u] = kmax[u];
-                row_hi[u] = kmax[u] ? rwin[u] : 64u;
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < JB; ++u) {
-          if (bb[u] < 0) continue;
-          const int b = bb[u];
-          const int64_t obase = static_cast<int64_t>(a.m0 + mm[u]) * a.nblk * a.kcand +
-                                static_cast<int64_t>(b) * a.kcand;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int slot = lane + 32 * h;
-            const uint32_t kk = h ? key_hi[u] : key_lo[u], rr = h ? row_hi[u] : row_lo[u];
-            if (slot < a.kcand) {
-              a.cand_val[obase + slot] = kk ? key_to_float(kk) : -INFINITY;
-              a.cand_id[obase + slot] = kk ? b * 64 + static_cast<int>(rr) : -1;
-            }
-          }
-        }
-      }
+      select_jobs(sw4, tile, keys);
       __syncwarp();
       if (lane == 0) mbar_arrive(keys_free);
     }
@@ -669,28 +750,29 @@ size_t coarse_wide_scratch_bytes(int64_t M, int64_t K) {
   const size_t kk = static_cast<size_t>(K);
   return round_up_sz(kWideMaxRows * kk * 2, 256) +          // B units
          round_up_sz(kWideMaxRows * (kk / 64) * 4, 256) +   // group sums (G >= 64)
-         round_up_sz(kWideMaxRows * 4, 256);                // exponents
+         round_up_sz(kWideMaxRows * 4, 256) +               // exponents
+         round_up_sz(static_cast<size_t>(kWMaxGrid) * kWRows * kWideMaxRows * 4, 256);  // keys
 }
 
 bool coarse_wide_supports(const CoarseCall& cc) {
   if (cc.bits != 2 || (cc.G != 64 && cc.G != 128) || cc.M <= kWideMinRows) return false;
-  if (cc.K % 512 != 0 || (cc.K / cc.G) % 8 != 0 || cc.K > 65536) return false;
+  if (cc.K % 512 != 0 || (cc.K / cc.G) % 8 != 0 || cc.K / cc.G > 80) return false;
   return encode_tiled_fn() != nullptr;
 }
 
 // Shared-memory plan of a pass; false if the rings do not fit.
 static bool plan_wide(WideArgs& a, int ncol, int G, int max_smem, int* smem_bytes) {
   const int cpj = G / 16;
-  a.unit_bytes = (cpj / 2) * 2 * ncol * 16;  // a B half-unit
+  a.unit_bytes = (cpj / 4) * 2 * ncol * 16;  // a B quarter-unit
   a.szp = a.KG * 2;
   const int sz_bytes = 2 * kWRows * a.szp;
-  const int key_bytes = kWRows * (ncol + 1) * 4;
+  const int key_bytes = 0;  // the key buffers live in the scratch
   const int xs_bytes = ncol * a.KG * 4;
   const int ew_bytes = ncol * 4;
-  const int bar_bytes = (2 * kWMaxNP + 2 * kWNB + 2 * kWMaxNA + 8 + 3) * 8 + 16;
+  const int bar_bytes = (2 * kWMaxNP + 2 * kWNB + 2 * kWMaxNA + 2 + 3) * 8 + 16;
   const int fixed = sz_bytes + key_bytes + xs_bytes + ew_bytes + bar_bytes + 64 + 1024;
-  // the B ring holds two half-units per issuer
-  const int nbu = kWNB;
+  // the B ring holds one and a half scale groups (kWNB quarters of four plane units)
+  const int nbu = kWNB * 4;
   int np = (max_smem - fixed - nbu * a.unit_bytes) / kWStageSmem;
   if (np > kWMaxNP) np = kWMaxNP;
   if (np < 3) return false;
@@ -779,6 +861,8 @@ cudaError_t launch_coarse_wide(const CoarseCall& cc, void* scratch, int num_sms,
   a.bbuf = bbuf;
   a.xs = xs;
   a.ew = ew;
+  a.keys_g = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(ew) +
+                                         round_up_sz(kWideMaxRows * 4, 256));
 
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.RB), static_cast<cuuint64_t>(a.N)};
@@ -791,7 +875,8 @@ cudaError_t launch_coarse_wide(const CoarseCall& cc, void* scratch, int num_sms,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  const int grid = a.ntiles < num_sms ? a.ntiles : num_sms;
+  int grid = a.ntiles < num_sms ? a.ntiles : num_sms;
+  if (grid > kWMaxGrid) grid = kWMaxGrid;
   const int64_t passes = (cc.M + kWideMaxRows - 1) / kWideMaxRows;
   for (int64_t ps = 0; ps < passes; ++ps) {
     // rows spread evenly over the passes, each a multiple of 16 columns wide

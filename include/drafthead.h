@@ -98,7 +98,8 @@ size_t dh_packed_bytes(int64_t N, int64_t K, int G, int bits);
  * must be ordered on one stream. The rerank needs the 256-byte header (status word) only. The
  * coarse pass of more than 16 hidden rows of an int2 head (its tensor-core path) also keeps its
  * scratch after the header: the hidden states laid out as the MMA operand (80 * K * 2 bytes),
- * their group sums and scales. */
+ * their group sums and scales, and the per-CTA buffers of coarse keys the block selection reads
+ * (256 * 128 * 80 * 4 bytes). */
 size_t dh_workspace_bytes(int64_t M, int64_t N, int64_t K, int kcand, int rerank);
 
 /*

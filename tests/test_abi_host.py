@@ -130,7 +130,7 @@ def test_workspace_bytes_sizes(lib):
     assert dh.dh_workspace_bytes(16, 124160, 5120, 8, 16) == 256
     r = lambda v: (v + 255) // 256 * 256
     assert dh.dh_workspace_bytes(72, 124160, 5120, 8, 16) == \
-        256 + r(80 * 5120 * 2) + r(80 * 80 * 4) + r(80 * 4)
+        256 + r(80 * 5120 * 2) + r(80 * 80 * 4) + r(80 * 4) + r(256 * 128 * 80 * 4)
     assert dh.dh_workspace_bytes(0, 124160, 5120, 8, 16) == 0
 
 
