@@ -216,6 +216,23 @@ def wide_range_rows(M: int, K: int, seed: int) -> np.ndarray:
     return bf16_bits(z)
 
 
+def wide_scale_range_head(W: np.ndarray, G: int, seed: int) -> np.ndarray:
+    """A head whose scale groups span a wide range within each row (bf16 bits [N, K] in and out):
+    every G-wide group of a row is multiplied by 2^-k, k drawn per (row, group) from
+    {0, 0, 0, 8, 16, 22, 26, 30}; row 0 keeps one group at full size and shrinks every other by
+    2^-30, and row 1 is shrunk by 2^-30 as a whole. Powers of two keep every bf16 exact."""
+    rng = np.random.default_rng(seed)
+    N, K = W.shape
+    kg = rng.choice(np.array([0, 0, 0, 8, 16, 22, 26, 30]), size=(N, K // G))
+    if N > 0:
+        kg[0] = 30
+        kg[0, rng.integers(K // G)] = 0
+    if N > 1:
+        kg[1] = 30
+    f = np.repeat(np.ldexp(1.0, -kg), G, axis=1)
+    return bf16_bits(bf16_value(W) * f)
+
+
 def fp8_head(W: np.ndarray):
     """An FP8 per-channel head built from a bf16 head (bit patterns uint16 [N, K]): the fp32
     row scale max|W[n]| / 448 and the e4m3 bytes of W / scale (round to nearest even, the
