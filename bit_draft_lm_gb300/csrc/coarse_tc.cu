@@ -90,9 +90,9 @@ struct WideArgs {
   int32_t* cand_id;
   uint16_t* y;  // bf16 [M, N] or nullptr
   uint32_t* status;
-  int np, nbu, unit_bytes, szp;
+  int np, unit_bytes, szp;
   uint32_t* keys_g;  // per-CTA key buffers [grid][128][NCOL] (scratch)
-  int off_bring, off_sz, off_keys, off_xs, off_ew, off_bars;
+  int off_bring, off_sz, off_xs, off_ew, off_bars;
 };
 
 __device__ __forceinline__ void w_cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -766,22 +766,19 @@ static bool plan_wide(WideArgs& a, int ncol, int G, int max_smem, int* smem_byte
   a.unit_bytes = (cpj / 4) * 2 * ncol * 16;  // a B quarter-unit
   a.szp = a.KG * 2;
   const int sz_bytes = 2 * kWRows * a.szp;
-  const int key_bytes = 0;  // the key buffers live in the scratch
   const int xs_bytes = ncol * a.KG * 4;
   const int ew_bytes = ncol * 4;
   const int bar_bytes = (2 * kWMaxNP + 2 * kWNB + 2 * kWMaxNA + 2 + 3) * 8 + 16;
-  const int fixed = sz_bytes + key_bytes + xs_bytes + ew_bytes + bar_bytes + 64 + 1024;
+  const int fixed = sz_bytes + xs_bytes + ew_bytes + bar_bytes + 64 + 1024;  // keys: in the scratch
   // the B ring holds one and a half scale groups (kWNB quarters of four plane units)
   const int nbu = kWNB * 4;
   int np = (max_smem - fixed - nbu * a.unit_bytes) / kWStageSmem;
   if (np > kWMaxNP) np = kWMaxNP;
   if (np < 3) return false;
   a.np = np;
-  a.nbu = nbu;
   a.off_bring = np * kWStageSmem;
   a.off_sz = a.off_bring + nbu * a.unit_bytes;
-  a.off_keys = a.off_sz + sz_bytes;
-  a.off_xs = a.off_keys + key_bytes;
+  a.off_xs = a.off_sz + sz_bytes;
   a.off_ew = a.off_xs + xs_bytes;
   a.off_bars = static_cast<int>(round_up_sz(a.off_ew + ew_bytes, 16));
   *smem_bytes = a.off_bars + bar_bytes + 1024;
