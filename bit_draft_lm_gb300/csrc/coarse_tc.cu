@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
       static_cast<int>(gridDim.x);
   const int total_stages = my_tiles * a.NS;
   const int quarters_per_tile = a.NJ * 4;  // B quarters of a tile: 4 per group
-  const int total_quarters = my_tiles * quarters_per_tile;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWMaxNP; ++i) {
@@ -351,34 +350,42 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
   int issued = 0, issued_b = 0;  // copies issued into the packed and B rings (warp 0, lane 0)
   if (warp == 0) {
-    // ---- one producer thread for both rings, in consumption order, never blocked on one ring
-    // while the other has room. The first packed stages go to L2 while the preceding kernel may
-    // still run (it may have written the weights: only L2, which is coherent, is touched before
-    // griddepcontrol.wait); every copy into shared memory comes after the wait.
+    // ---- one producer thread for both rings, in one fixed order: packed stage gs + np - 1,
+    // then the B quarters of stage gs. Every wait is a suspended, bounded mbarrier wait (no
+    // polling: the thread shares its SMSP with a dequantising warp). The order cannot deadlock:
+    // a packed slot comes back once the dequantising warps finish stage gs - 1, whose A stages
+    // need only MMAs on B quarters already issued; a B slot comes back once its issuer passes a
+    // quarter six back, whose A stages need only packed stages already issued. The first packed
+    // stages go to L2 while the preceding kernel may still run (it may have written the weights:
+    // only L2, which is coherent, is touched before griddepcontrol.wait); every copy into shared
+    // memory comes after the wait.
     if (lane == 0) {
       for (int s = 0; s < np && s < total_stages; ++s)
         tma_prefetch_l2_2d(&tmap, (s % a.NS) * kWStageBytes, tile_of(s / a.NS) * kWRows);
       grid_dependency_wait();
-      int pslot = 0, ps_in_tile = 0, plt = 0, bslot = 0, bunit = 0;
+      constexpr int kQPS = 8 / CPQ;  // B quarters per packed stage (a stage is 8 chunks)
+      int pslot = 0, bslot = 0, bunit = 0, p_st = 0, p_lt = 0;
       uint32_t pph = 0u, bph = 0u;
-      uint64_t t_idle = 0;
-      while ((issued < total_stages || issued_b < total_quarters) && !*abort_flag) {
-        bool progress = false;
-        if (issued < total_stages &&
-            (issued < np || mbar_test_wait(&pempty[pslot], pph ^ 1u))) {
+      // step gs issues packed stage gs + np - 1 and then stage gs's B quarters (steps before 0
+      // only fill the packed ring)
+      for (int gs = 1 - np; gs < total_stages && !*abort_flag; ++gs) {
+        if (issued < total_stages) {
+          if (issued >= np) wait_bar(&pempty[pslot], pph ^ 1u);
+          if (*abort_flag) break;
           mbar_arrive_expect_tx(&pfull[pslot], static_cast<uint32_t>(kWStageSmem));
-          tma_load_2d(sm + pslot * kWStageSmem, &tmap, ps_in_tile * kWStageBytes,
-                      tile_of(plt) * kWRows, &pfull[pslot]);
+          tma_load_2d(sm + pslot * kWStageSmem, &tmap, p_st * kWStageBytes,
+                      tile_of(p_lt) * kWRows, &pfull[pslot]);
           advance(pslot, pph, np);
-          if (++ps_in_tile == a.NS) {
-            ps_in_tile = 0;
-            ++plt;
+          if (++p_st == a.NS) {
+            p_st = 0;
+            ++p_lt;
           }
           ++issued;
-          progress = true;
         }
-        if (issued_b < total_quarters &&
-            (issued_b < kWNB || mbar_test_wait(&bempty[bslot], bph ^ 1u))) {
+        if (gs < 0) continue;
+        for (int k = 0; k < kQPS && !*abort_flag; ++k) {
+          if (issued_b >= kWNB) wait_bar(&bempty[bslot], bph ^ 1u);
+          if (*abort_flag) break;
           // quarter (J, uq): the prep layout is (J, plane, chunk), so the quarter is four
           // contiguous plane units, one copy each, landing side by side in the slot
           const int uj = bunit >> 2, uq = bunit & 3;
@@ -391,19 +398,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
           advance(bslot, bph, kWNB);
           if (++bunit == quarters_per_tile) bunit = 0;
           ++issued_b;
-          progress = true;
-        }
-        if (progress) {
-          t_idle = 0;
-        } else {
-          const uint64_t now = global_timer_ns();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > kWaitLimitNs) {
-            *abort_flag = 1;
-            set_status(a.status, DH_DEV_WAIT_TIMEOUT);
-          }
-          __nanosleep(64);
         }
       }
     }
