@@ -78,6 +78,7 @@ COARSE_CASES = [
     (40, 5120, 20000, 128, 2, 3, 24),   # K = 5120, 48 columns, odd KCAND
     (97, 1024, 3000, 128, 2, 8, 25),    # two passes (48 + 49 rows)
     (72, 5120, 124160, 128, 2, 8, 26),  # the vocabulary-scale head at 72 rows
+    (20, 1024, 4100, 128, 2, 64, 33),   # KCAND = 64: candidates past the 32nd slot
     # the hidden size of the vocabulary-scale head compiled in (K = 5120) for every variant the
     # bench times: its shared-memory plans and ring depths depend on K, M, bits and G, not on N
     (8, 5120, 20000, 128, 4, 1, 27),    # int4, G = 128, KCAND = 1 (the 4-bit comparison head)
