@@ -61,7 +61,7 @@ constexpr int kWDeqWarps = 8;   // dequantising: two per TMEM lane quadrant
 constexpr int kWFoldWarps = 8;  // fold: two per TMEM lane quadrant
 constexpr int kWSelWarps = 3;   // block top-KCAND selection (off the critical path)
 constexpr int kWSelWorkers = kWSelWarps + kWFoldWarps;  // the fold warps take a share too
-constexpr int kWIssuers = 3;    // MMA-issuing threads: chunk c goes to issuer c % 3
+constexpr int kWIssuers = 3;    // MMA-issuing threads: B quarter Q goes to issuer Q % 3
 // warp 0: the copy producer (one thread, both rings); warps 1 .. 3: the MMA issuers; then the
 // dequantising, fold and selection warps
 constexpr int kWDeq0 = 1 + kWIssuers;          // first dequantising warp
