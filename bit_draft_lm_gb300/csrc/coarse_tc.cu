@@ -202,9 +202,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
   uint64_t* pfull = reinterpret_cast<uint64_t*>(sm + a.off_bars);  // [kWMaxNP] stage landed
   uint64_t* pempty = pfull + kWMaxNP;   // [kWMaxNP] stage read by the dequantising warps
   uint64_t* bfull = pempty + kWMaxNP;   // [kWNB] B quarter landed (four plane units)
-  uint64_t* bempty = bfull + kWNB;      // [kWNB] every issuer past the quarter
-  uint64_t* afull = bempty + kWNB;      // [kWMaxNA] A stage written
-  uint64_t* aempty = afull + kWMaxNA;   // [kWMaxNA] A stage's MMAs done
+  uint64_t* bempty = bfull + kWNB;      // [kWNB] the quarter's issuer past it
+  uint64_t* afull = bempty + kWNB;      // [NAQ used] a quarter's A stages written
+  uint64_t* aempty = afull + kWMaxNA;   // [NAQ used] ... and its MMAs done
   uint64_t* dfull = aempty + kWMaxNA;   // the tile's D slots complete
   uint64_t* dempty = dfull + 1;         // ... and read by the fold warps
   uint64_t* mma_done = dempty + 1;      // every MMA of the CTA complete
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   };
 
   // block top-KCAND of this worker's share of a tile's jobs (job j = (64-row block j / R of the
-  // tile, hidden row j % R)), from the tile's keys [128][PITCH]; a warp runs JB jobs at once so
+  // tile, hidden row j % R)), from the tile's keys [NCOL][128]; a warp runs JB jobs at once so
   // that their warp reductions overlap (each round of one job is a chain of two)
   auto select_jobs = [&](int worker, int tile, const uint32_t* keys) {
     constexpr int JB = 4;
