@@ -456,7 +456,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // byte positions as f16 pairs c S 2^e: per pair one LOP3 puts the two codes (times 4^p) into
     // the mantissa of 1.0, one HFMA2 with the group's multiplier M = S 2^(e + 10 - 2p) and -M
     // leaves exactly c S 2^e (the FMA rounds once, and the product has at most 10 significant
-    // bits).
+    // bits) whenever S 2^e >= 2^-17, i.e. for every scale of at least 2^-20 of the row's largest;
+    // below that it is off by less than one f16 subnormal step.
     const int sub = (warp - kWDeq0) >> 2;  // chunk parity of this warp
     const int row = (warp & 3) * 32 + lane;
     const uint32_t my_a = a_base + tmem_lane_base(warp);

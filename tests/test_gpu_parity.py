@@ -527,7 +527,7 @@ def test_wide_scale_range_head(M, G):
     """A head whose group scales span up to ~2^25 within a row (groups shrunk by up to 2^-30;
     the quantiser's 1e-8 scale floor caps the spread). The tensor-core pass (M > 16) writes each
     code times its scale into the MMA operand relative to the row's largest scale, exactly while
-    a scale is at least ~2^-21 of it; below that the small groups' share rounds in f16, which
+    a scale is at least 2^-20 of it; below that the small groups' share rounds in f16, which
     must stay inside the coarse tolerance like everything else. M=3 runs the warp-MMA pass."""
     K, N, kcand, R = 5120, 8192, 8, 16
     w = synth.make_workload(M, K, N, 150 + M, plant=True)
