@@ -78,3 +78,29 @@ def test_ratio_bound_holds_for_any_largest_scale():
             for p in range(4):
                 for c in range(4):
                     assert _dequant(c, p, s * 2.0 ** e) == c * s * 2.0 ** e
+
+
+def test_fold_formula_matches_the_oracle():
+    """The whole pass's arithmetic, with the kernel's operands: A = c S 2^e (exact, above), B = the
+    f16 x 2^(15 - E_m), D = sum A B (here in fp64), then the fold D 2^(E_m - e - 17) plus the
+    zero-point part sum_g (S - ZS) XS. That must be the page's coarse value (the oracle's), so the
+    exponent offsets are right."""
+    import oracle
+    from bit_draft_lm_gb300 import synth
+    M, K, N, G = 3, 1024, 64, 128
+    w = synth.make_workload(M, K, N, 41, plant=False)
+    packed, S, ZS = oracle.quantize_pack(w.W, G, 2)
+    codes = oracle.unpack_codes(packed, K, 2).astype(np.float64)          # [N, K]
+    Sv = synth.bf16_value(S).astype(np.float64)                          # [N, K/G]
+    ZSv = synth.bf16_value(ZS).astype(np.float64)
+    x = synth.bf16_value(w.x).astype(np.float64)                         # [M, K]
+    e = np.array([_scale_exponent(int(np.max(S[n] & 0x7FFF))) for n in range(N)])
+    A = codes * np.repeat(Sv, G, axis=1) * (2.0 ** e)[:, None]
+    Em = np.array([(int(np.max(w.x[m] & 0x7FFF)) >> 7) - 126 for m in range(M)])
+    B = np.stack([np.float16(x[m] * 2.0 ** (15 - Em[m])).astype(np.float64) for m in range(M)])
+    D = B @ A.T                                                          # [M, N]
+    XS = x.reshape(M, K // G, G).sum(axis=2)                             # [M, K/G]
+    c = D * 2.0 ** (Em[:, None] - e[None, :] - 17) + XS @ (Sv - ZSv).T
+    ref = oracle.coarse(w.x, packed, S, ZS, G, 2)
+    scale = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    assert np.max(np.abs(c - ref) / scale) < 1e-9
