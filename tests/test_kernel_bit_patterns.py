@@ -69,3 +69,40 @@ def test_every_byte_value():
                 got = lo[0] if slot < 2 else hi[0]
                 other = hi[0] if slot < 2 else lo[0]
                 assert got == want and other == 0.0
+
+
+@pytest.mark.parametrize("bits,G", [(2, 128), (2, 64), (4, 128), (4, 64)])
+def test_warp_mma_scaling_constants_match_the_oracle(bits, G):
+    """The warp-MMA pass's operands and scale factors, composed in fp64: A = code 2^(s - 24) (the
+    f16 subnormals above), B = f16(x 2^(15 - E - s)) with E from the largest |x| of the warp's
+    strip (64 packed bytes of every plane), and each partial times S_g 2^(E + 9 - log2 L)
+    (L = 4 for int2, 16 for int4), plus the zero-point part sum_g (S - ZS) XS: that is the page's
+    coarse value (the oracle's), so the exponent offsets are right."""
+    M, K, N = 3, 2048, 64
+    w = synth.make_workload(M, K, N, 51 + bits + G, plant=False)
+    packed, S, ZS = oracle.quantize_pack(w.W, G, bits)
+    codes = oracle.unpack_codes(packed, K, bits).astype(np.float64)      # [N, K]
+    Sv = synth.bf16_value(S).astype(np.float64)
+    ZSv = synth.bf16_value(ZS).astype(np.float64)
+    x = synth.bf16_value(w.x).astype(np.float64)
+    RB = K * bits // 8
+    k = np.arange(K)
+    plane, byte = k // RB, k % RB
+    shift = bits * plane
+    strip = byte // 64
+    logL = 2 if bits == 2 else 4
+    A = codes * 2.0 ** (shift - 24)                                      # [N, K]
+    c = np.zeros((M, N))
+    for m in range(M):
+        E = np.zeros(K, dtype=np.int64)
+        for j in range(RB // 64):
+            sel = strip == j
+            mx = int(np.max(w.x[m][sel] & 0x7FFF))
+            E[sel] = min(max((mx >> 7) - 126, -100), 100)
+        B = np.float16(x[m] * 2.0 ** (15 - E - shift)).astype(np.float64)
+        c[m] = (A * B * 2.0 ** (E + 9 - logL) * np.repeat(Sv, G, axis=1)).sum(axis=1)
+    XS = x.reshape(M, K // G, G).sum(axis=2)
+    c += XS @ (Sv - ZSv).T
+    ref = oracle.coarse(w.x, packed, S, ZS, G, bits)
+    scale = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    assert np.max(np.abs(c - ref) / scale) < 1e-9
